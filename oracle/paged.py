@@ -1,0 +1,145 @@
+"""Paged KV pool: byte layout, scatter of new tokens, gather of a sequence.
+Test infrastructure only (see ``oracle/__init__.py``).
+
+The pages describe the pool only as fixed-size blocks in one shared pool
+sized at start-up and not divided among request lanes ("ninfer-windows-tp2"
+README, section "Current limits"), with a head-major ("HND") layout inside a
+block ("262,144 Tokens on One RTX 5090 ...", section "The stack, for the
+impatient").  The byte layout below is this library's own choice; it is the
+definition the GPU encoder is checked against, byte for byte.
+
+A page holds PAGE = 16 consecutive token positions of one sequence.  Token t
+of sequence b lives in page ``page_table[b][t // 16]``, slot ``t % 16``.
+Inside a page the record of each KV head h is contiguous, heads in order:
+
+  NVFP4 (4,608 bytes per page-head, D = 256):
+    K codes   [16 slots][D/2 bytes]   element 2k in the low nibble of byte k
+    K scales  [16 slots][D/16 bytes]  E4M3, one per 16 contiguous elements
+    V codes   [16 slots][D/2 bytes]
+    V scales  [16 slots][D/16 bytes]
+  bf16 (16,384 bytes per page-head):
+    K [16 slots][D] bf16 (little-endian), then V [16 slots][D] bf16
+"""
+import numpy as np
+
+from .formats import bf16_bits, bf16_from_bits
+from .nvfp4 import dequantize, pack_nibbles, quantize, unpack_nibbles
+
+PAGE = 16
+NVFP4 = "nvfp4"
+BF16 = "bf16"
+
+
+def page_head_bytes(dtype, head_dim):
+    if dtype == NVFP4:
+        return 2 * PAGE * (head_dim // 2 + head_dim // 16)
+    return 2 * PAGE * head_dim * 2
+
+
+def page_bytes(dtype, num_kv_heads, head_dim):
+    return num_kv_heads * page_head_bytes(dtype, head_dim)
+
+
+def _sections(dtype, head_dim):
+    """(offset, row_bytes) of K-data, K-scale, V-data, V-scale sections."""
+    if dtype == NVFP4:
+        cb, sb = head_dim // 2, head_dim // 16
+        k0 = 0
+        ks = k0 + PAGE * cb
+        v0 = ks + PAGE * sb
+        vs = v0 + PAGE * cb
+        return (k0, cb), (ks, sb), (v0, cb), (vs, sb)
+    rb = head_dim * 2
+    return (0, rb), None, (PAGE * rb, rb), None
+
+
+def new_pool(num_pages, dtype, num_kv_heads, head_dim):
+    return np.zeros((num_pages, page_bytes(dtype, num_kv_heads, head_dim)), dtype=np.uint8)
+
+
+def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, pos_of_tok,
+                   k, v, g_k=None, g_v=None):
+    """Write new tokens into the pool.
+
+    ``k``, ``v``: bf16-valued float arrays [T, Hkv, D] (K already roped).
+    For NVFP4 they are quantised with per-tensor decode scales g_k, g_v.
+    Returns the pool (modified in place)."""
+    phb = page_head_bytes(dtype, head_dim)
+    (k0, kb), ks, (v0, vb), vs = _sections(dtype, head_dim)
+    if dtype == NVFP4:
+        kq, kscale = quantize(k, g_k)
+        vq, vscale = quantize(v, g_v)
+        krow, vrow = pack_nibbles(kq), pack_nibbles(vq)
+    else:
+        krow = bf16_bits(k).view(np.uint8).reshape(k.shape[0], num_kv_heads, -1)
+        vrow = bf16_bits(v).view(np.uint8).reshape(v.shape[0], num_kv_heads, -1)
+    for t in range(len(seq_of_tok)):
+        b, p = int(seq_of_tok[t]), int(pos_of_tok[t])
+        page = int(page_table[b][p // PAGE])
+        slot = p % PAGE
+        for h in range(num_kv_heads):
+            base = h * phb
+            pool[page, base + k0 + slot * kb: base + k0 + (slot + 1) * kb] = krow[t, h]
+            pool[page, base + v0 + slot * vb: base + v0 + (slot + 1) * vb] = vrow[t, h]
+            if dtype == NVFP4:
+                (ko, ksb), (vo, vsb) = ks, vs
+                pool[page, base + ko + slot * ksb: base + ko + (slot + 1) * ksb] = kscale[t, h]
+                pool[page, base + vo + slot * vsb: base + vo + (slot + 1) * vsb] = vscale[t, h]
+    return pool
+
+
+def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, start_pos, k, v,
+                          g_k=None, g_v=None):
+    """Write tokens start_pos .. start_pos+T-1 of one sequence (vectorised
+    form of ``scatter_tokens`` for long fills; same bytes)."""
+    T = k.shape[0]
+    phb = page_head_bytes(dtype, head_dim)
+    (k0, kb), ks, (v0, vb), vs = _sections(dtype, head_dim)
+    pos = start_pos + np.arange(T)
+    pages = np.asarray(pages_of_seq)[pos // PAGE]
+    slots = pos % PAGE
+    if dtype == NVFP4:
+        kq, kscale = quantize(k, g_k)
+        vq, vscale = quantize(v, g_v)
+        krow, vrow = pack_nibbles(kq), pack_nibbles(vq)
+    else:
+        krow = bf16_bits(k).view(np.uint8).reshape(T, num_kv_heads, -1)
+        vrow = bf16_bits(v).view(np.uint8).reshape(T, num_kv_heads, -1)
+    for h in range(num_kv_heads):
+        base = h * phb
+        for j in range(kb):
+            pool[pages, base + k0 + slots * kb + j] = krow[:, h, j]
+            pool[pages, base + v0 + slots * vb + j] = vrow[:, h, j]
+        if dtype == NVFP4:
+            (ko, ksb), (vo, vsb) = ks, vs
+            for j in range(ksb):
+                pool[pages, base + ko + slots * ksb + j] = kscale[:, h, j]
+                pool[pages, base + vo + slots * vsb + j] = vscale[:, h, j]
+    return pool
+
+
+def gather_sequence(pool, dtype, num_kv_heads, head_dim, pages_of_seq, seq_len, head,
+                    g_k=None, g_v=None, start=0):
+    """Dequantised K, V of one sequence and KV head, tokens start..seq_len-1,
+    as float64 [L, D] each.  Token t is read from page pages_of_seq[t // 16],
+    slot t % 16."""
+    phb = page_head_bytes(dtype, head_dim)
+    (k0, kb), ks, (v0, vb), vs = _sections(dtype, head_dim)
+    t = np.arange(start, seq_len)
+    pages = np.asarray(pages_of_seq)[t // PAGE]
+    slots = t % PAGE
+    base = head * phb
+    kcols = base + k0 + slots[:, None] * kb + np.arange(kb)[None, :]
+    vcols = base + v0 + slots[:, None] * vb + np.arange(vb)[None, :]
+    krow = pool[pages[:, None], kcols]
+    vrow = pool[pages[:, None], vcols]
+    if dtype == NVFP4:
+        (ko, ksb), (vo, vsb) = ks, vs
+        kscol = base + ko + slots[:, None] * ksb + np.arange(ksb)[None, :]
+        vscol = base + vo + slots[:, None] * vsb + np.arange(vsb)[None, :]
+        kk = dequantize(unpack_nibbles(krow), pool[pages[:, None], kscol], g_k)
+        vv = dequantize(unpack_nibbles(vrow), pool[pages[:, None], vscol], g_v)
+        return kk, vv
+    kk = bf16_from_bits(krow.view(np.uint16))
+    vv = bf16_from_bits(vrow.view(np.uint16))
+    return kk, vv

@@ -1,0 +1,347 @@
+"""Benchmark of the paged NVFP4 decode step on GB300.
+
+One step = the whole decode path for one new token of the million-token
+workload (1 sequence, 1,048,576 keys after the append, 24 query / 4 KV heads
+of dim 256, YaRN x4, NVFP4 pool in 16-token pages randomly permuted):
+
+    kv_append_nvfp4 -> paged_decode_attention -> split_kv_combine
+
+(the YaRN table is built once, before timing).  ``value`` is KV tokens per
+second per layer with inputs resident in HBM; the pool (1.2 GB) is far
+larger than L2, so no flush is needed between steps.  ``e2e`` times the same
+step through the public API with the step's inputs (q, k, v of the new
+token) copied from pinned host memory and the bf16 output copied back.
+
+``--impl reference`` times the CPU oracle (float64 NumPy) on the host cores
+instead, on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "1M-ctx paged decode attention: KV tokens/s/layer and HBM GB/s (% of GB300 peak)"
+UNIT = "KV tokens/s/layer"
+FALLBACK_HBM_GBS = 6800.0   # earlier GB300 copy measurement, used if no measured peaks file
+ALGO_BYTES_PER_TOKEN = {"nvfp4": 4 * 2 * (128 + 16), "bf16": 4 * 2 * 256 * 2}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", type=int, default=3, help="workload number (1..4)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if key in d:
+                return float(d[key]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload(cfg):
+    from paged_nvfp4_kv_gb300 import workloads as W
+    return W.CONFIGS[cfg]()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+
+def oracle_rate(w, seconds, max_keys=None):
+    """KV tokens/s/layer of the float64 oracle on the host cores: rope and
+    encode the sampled keys (untimed), then time the oracle's paged
+    attention of all query rows of sequence 0 over a sample of its keys,
+    sized to take about ``seconds``."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle_path
+    from oracle import attention as OA
+    from oracle import paged as OP
+    from oracle import yarn as OY
+
+    L = int(w.seq_lens[0])
+    dtype = OP.NVFP4 if w.kv_dtype == "nvfp4" else OP.BF16
+    R = w.yarn["rotary_dim"]
+
+    def run(n):
+        cos_t, sin_t = OY.rope_tables(w.yarn, L)
+        npg = (n + 15) // 16
+        pool = OP.new_pool(npg, dtype, w.num_kv_heads, w.head_dim)
+        table = np.arange(npg, dtype=np.int32)
+        k = w.k_rows(0, L - n, L).astype(np.float64)
+        v = w.v_rows(0, L - n, L).astype(np.float64)
+        kr = OY.rope_rows(k, np.arange(L - n, L), cos_t, sin_t, R)
+        OP.scatter_sequence_fast(pool, dtype, w.num_kv_heads, w.head_dim, table, 0, kr, v, w.g_k,
+                                 w.g_v)
+        q = oracle_path.roped_new_q(w, cos_t, sin_t)[: int(w.qlen[0])]
+        t0 = time.perf_counter()
+        OA.paged_decode(pool, dtype, w.num_kv_heads, w.head_dim, q, np.array([0, q.shape[0]]),
+                        table[None, :], np.array([n]), w.num_q_heads, True, w.g_k, w.g_v)
+        return time.perf_counter() - t0
+
+    n = min(L, 16384)
+    dt = run(n)
+    target = max(n, min(L if max_keys is None else max_keys, int(n * seconds / max(dt, 1e-3))))
+    target = (target // 16) * 16 or 16
+    if target > n:
+        n = target
+        dt = run(n)
+    return n / dt, n, dt
+
+
+def cpu_info():
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return cores
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workload(args.config)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    times = []
+    keys = None
+    for i in range(args.warmup + args.steps):
+        rate, n, dt = oracle_rate(w, per_step)
+        keys = n
+        if i >= args.warmup:
+            times.append(dt)
+    rate = keys / float(np.mean(times))
+    cores = cpu_info()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "keys": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d of %d keys of sequence 0, all %d query heads, per step"
+                                   % (keys, int(w.seq_lens[0]), w.num_q_heads)},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+def run_ours(args):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_nvfp4_kv_gb300 import paged_decode_attention, split_kv_combine
+    from paged_nvfp4_kv_gb300.engine import DecodeSession
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = workload(args.config)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        s = DecodeSession(w, device="cuda", stream=stream)
+        s.fill()
+    torch.cuda.synchronize()
+
+    # events around each call of the step, on the launching stream
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            s.step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    with clocks:
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(K):
+                ev[i][0].record(stream)
+                s.append()
+                ev[i][1].record(stream)
+                w_ = s.w
+                paged_decode_attention(s.cache, s.q_roped, s.qo_indptr, s.page_table, s.seq_lens,
+                                       w_.num_q_heads, s.max_qlen, s.sm_scale, w_.causal, s.o_part,
+                                       s.lse_part, s.work_meta, s.dev_err, stream)
+                ev[i][2].record(stream)
+                split_kv_combine(s.o_part, s.lse_part, s.work_meta, s.qo_indptr, s.total_q,
+                                 w_.num_q_heads, w_.num_kv_heads, s.max_qlen, s.out, s.lse, stream)
+                ev[i][3].record(stream)
+            stop.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+    total_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    append_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    combine_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
+    ms_per_step = total_ms / K
+    keys = int(w.seq_lens.sum())
+    value = world * keys / (ms_per_step * 1e-3)
+    err = s.error_word()
+
+    # ---- end to end through the public API, host buffers
+    qh = s.q.cpu().pin_memory()
+    kh = s.k.cpu().pin_memory()
+    vh = s.v.cpu().pin_memory()
+    out_h = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
+    h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2
+    d2h = out_h.numel() * 2
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            s.q.copy_(qh, non_blocking=True)
+            s.k.copy_(kh, non_blocking=True)
+            s.v.copy_(vh, non_blocking=True)
+            s.step()
+            out_h.copy_(s.out, non_blocking=True)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            s.q.copy_(qh, non_blocking=True)
+            s.k.copy_(kh, non_blocking=True)
+            s.v.copy_(vh, non_blocking=True)
+            s.step()
+            out_h.copy_(s.out, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * keys / (e2e_ms * 1e-3)
+
+    peak, peak_kind = peaks()
+    algo_bytes = keys * ALGO_BYTES_PER_TOKEN[w.kv_dtype]
+    achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16-mma/fp32-softmax over %s KV" % w.kv_dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "keys": keys, "kv_dtype": w.kv_dtype,
+                   "query_rows": int(w.total_q) * w.num_q_heads, "heads": "24q/4kv x 256",
+                   "pages": int(w.num_pages), "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "kernels_ms": {"kv_append_nvfp4": append_ms, "paged_decode_attention": decode_ms,
+                       "split_kv_combine": combine_ms},
+        "hbm_gbs_decode": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "paged_decode_attention",
+                     "algorithmic_bytes_per_launch": algo_bytes},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(),
+        "dev_err": err,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, dt = oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_info(), "kind": "oracle",
+                                "sample": "%d of %d keys of sequence 0, all %d query heads"
+                                          % (n, int(w.seq_lens[0]), w.num_q_heads),
+                                "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

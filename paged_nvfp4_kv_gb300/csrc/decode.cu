@@ -1,0 +1,875 @@
+// paged_decode_attention: split-KV GQA decode over the paged pool.
+//
+// The attention is the plain softmax(q k^T * sm_scale) v of every new query
+// row over the keys of its sequence (causal inside the new rows), evaluated
+// in key splits whose partials are merged by split_kv_combine ("NInfer --
+// Windows 11 TP2 fork" README, section "Limitations": the decode key range
+// is split; "A 1,048,576-token context on two RTX 5090s", section "Things
+// that bit me": no compile-time ceiling on the number of keys -- nothing here
+// is sized by the context length).
+//
+// Work decomposition (stream-K).  The unit of work is one (sequence b, KV
+// head h, page) triple: 16 tokens of one head, 4,608 bytes NVFP4 or 16 KiB
+// bf16, read exactly once per call and shared by all the head's query rows
+// (GQA).  Units are ordered (b, h, page) and the whole list is cut into
+// gridDim.x equal contiguous ranges, one per CTA, gridDim.x = SM count; a
+// CTA's range meets at most a few (b, h) segments and writes one partial per
+// segment piece into slot (segment + CTA index), which is injective.
+//
+// Inside a CTA: warp 8 produces, warps 0..7 consume.  The producer walks the
+// CTA's units, reads their page ids from the page table and issues one 2-D
+// TMA load per unit (the head record as 36 or 128 rows of 128 bytes, 128-byte
+// swizzle) into a ring of shared-memory stages guarded by full/empty
+// mbarriers.  Consumer warp w takes every (8/RG)-th unit; for RG > 1 the RG
+// warps of a group split the query rows of the same unit.  Per unit a warp
+// computes S^T = K Q^T with m16n8k16 tensor-core MMAs (16 tokens of the page
+// are the M dimension, query rows the N dimension, so GQA rows pad only to
+// 8), keeps an online softmax per query row, and accumulates O^T += V^T P^T
+// (head dims as M).  NVFP4 codes are widened in registers: E2M1 -> fp16 and
+// times the E4M3 block scale, both exact in fp16; the per-tensor scales fold
+// into the logit scale (K) and the output (V).  P is rounded to fp16 for the
+// P.V product.  At the end of each segment piece the consumer warps merge
+// their (m, l, O) in shared memory in a fixed order (deterministic) and write
+// the normalised partial and its natural-log LSE.
+#include <cmath>
+
+#include <cudaTypedefs.h>
+
+#include "device_common.cuh"
+#include "host_common.h"
+
+namespace pnkv {
+namespace {
+
+// A CTA is one warpgroup pair (8 warps, 256 threads): register allocation
+// is per 4-warp group, so 8 warps keep the full 255 registers per thread.
+// One warp produces; the consumers are the largest multiple of RG below 8.
+constexpr int kThreads = 256;
+constexpr int kProducerWarp = 7;
+template <int RG>
+struct Consumers {
+  static constexpr int kWarps = (7 / RG) * RG;
+  static constexpr int kThreads = kWarps * 32;
+};
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct DecodeArgs {
+  int64_t num_pages;
+  int32_t hkv;
+  int32_t group;          // query heads per KV head
+  float qk_scale_log2;    // sm_scale * log2(e) (* k_scale for NVFP4)
+  float out_scale;        // v_scale for NVFP4, 1 for bf16
+  const uint16_t* q;      // roped bf16 queries [total_q, hq, 256]
+  const int32_t* qo_indptr;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t hq;
+  int32_t max_qlen;
+  int32_t rows_per_slot;  // group * max_qlen
+  int32_t causal;
+  float* o_part;
+  float* lse_part;
+  int64_t part_slots;
+  int32_t* work_meta;
+  int32_t* dev_err;
+};
+
+template <int KVDT>
+struct Geometry;
+template <>
+struct Geometry<PNKV_KV_NVFP4> {
+  static constexpr int kBoxRows = 36;      // 4,608 B head record
+  static constexpr int kStageBytes = 5120; // next multiple of 1,024
+  static constexpr uint32_t kTxBytes = 4608;
+};
+template <>
+struct Geometry<PNKV_KV_BF16> {
+  static constexpr int kBoxRows = 128;     // 16,384 B head record
+  static constexpr int kStageBytes = 16384;
+  static constexpr uint32_t kTxBytes = 16384;
+};
+
+// ---------------------------------------------------------------------------
+// Sequence walk: unit counts per sequence and the segment containing a unit.
+// Every thread of a CTA runs the same walk, so all agree on the pieces.
+
+struct SeqInfo {
+  int32_t len;    // keys
+  int32_t qlen;   // new query rows (tokens)
+  int32_t q0;     // qo_indptr[b]
+  int32_t pages;  // units per (b, h); 0 if the sequence has no valid work
+};
+
+__device__ __forceinline__ SeqInfo load_seq(const DecodeArgs& a, int b, bool flag) {
+  SeqInfo s;
+  s.len = __ldg(a.seq_lens + b);
+  s.q0 = __ldg(a.qo_indptr + b);
+  s.qlen = __ldg(a.qo_indptr + b + 1) - s.q0;
+  s.pages = (s.len + 15) >> 4;
+  bool ok = true;
+  if (s.qlen < 0 || s.qlen > a.max_qlen || s.qlen > s.len || s.q0 < 0) {
+    if (flag) flag_error(a.dev_err, PNKV_DEV_ERR_QO_INDPTR);
+    ok = false;
+  }
+  if (s.len < 0 || static_cast<int64_t>(s.pages) > a.pt_stride) {
+    if (flag) flag_error(a.dev_err, PNKV_DEV_ERR_SEQ_LEN);
+    ok = false;
+  }
+  if (!ok || s.qlen == 0) s.pages = 0;
+  return s;
+}
+
+// Total units over all sequences (warp-cooperative; every lane gets it).
+__device__ __forceinline__ int64_t total_units(const DecodeArgs& a, int lane) {
+  int64_t tot = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int64_t u = 0;
+    if (b < a.batch) u = static_cast<int64_t>(load_seq(a, b, true).pages) * a.hkv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+    tot += u;
+  }
+  return tot;
+}
+
+// Find the sequence b whose unit range [base, base + hkv * pages) contains
+// `u` (warp-cooperative).  Returns b and its base.
+__device__ __forceinline__ void find_seq(const DecodeArgs& a, int64_t u, int lane, int* b_out,
+                                         int64_t* base_out) {
+  int64_t base = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int64_t cnt = 0;
+    if (b < a.batch) cnt = static_cast<int64_t>(load_seq(a, b, false).pages) * a.hkv;
+    // inclusive scan
+    int64_t inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, b < a.batch && base + inc > u);
+    if (hit) {
+      const int first = __ffs(hit) - 1;
+      const int64_t excl = __shfl_sync(0xffffffffu, inc - cnt, first);
+      *b_out = b0 + first;
+      *base_out = base + excl;
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  *b_out = a.batch;
+  *base_out = base;
+}
+
+// A maximal run of this CTA's units inside one (b, h) segment.
+struct Piece {
+  int b, h;
+  SeqInfo s;
+  int64_t seg_start;  // flattened unit index of the segment's first unit
+  int32_t p0;         // first page (index within the sequence)
+  int32_t n;          // units in this piece
+  int64_t i0;         // CTA-local index of the piece's first unit
+};
+
+struct Walker {
+  int b, h;
+  SeqInfo s;
+  int64_t seg_start;
+  int64_t u, u_end, u_begin;
+  bool valid;
+
+  __device__ void init(const DecodeArgs& a, int64_t begin, int64_t end, int lane) {
+    u_begin = u = begin;
+    u_end = end;
+    valid = begin < end;
+    if (!valid) return;
+    int64_t base;
+    find_seq(a, begin, lane, &b, &base);
+    s = load_seq(a, b, false);
+    h = static_cast<int>((begin - base) / s.pages);
+    seg_start = base + static_cast<int64_t>(h) * s.pages;
+  }
+
+  // Next piece; false when the CTA's range is done.
+  __device__ bool next(const DecodeArgs& a, Piece* pc) {
+    if (!valid || u >= u_end) return false;
+    while (u >= seg_start + s.pages) {  // advance to the segment holding u
+      seg_start += s.pages;
+      if (++h == a.hkv) {
+        h = 0;
+        ++b;
+        s = load_seq(a, b, false);
+      }
+    }
+    pc->b = b;
+    pc->h = h;
+    pc->s = s;
+    pc->seg_start = seg_start;
+    pc->p0 = static_cast<int32_t>(u - seg_start);
+    const int64_t stop = min(u_end, seg_start + s.pages);
+    pc->n = static_cast<int32_t>(stop - u);
+    pc->i0 = u - u_begin;
+    u = stop;
+    return true;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Shared memory plan.
+
+template <int KVDT, int NTW, int RG>
+struct Plan {
+  static constexpr int kStreams = Consumers<RG>::kWarps / RG;   // warps that split the units
+  static constexpr int kRows = 8 * NTW * RG;             // query rows per KV head handled
+  static constexpr int kMergeBytes = kRows * 256 * 4;
+  static constexpr int kMlBytes = kStreams * kRows * 2 * 4;
+  static constexpr int kFixed = kMergeBytes + kMlBytes + 1024 /*align*/ + 1024 /*bars, flags*/;
+  static constexpr int kMaxSmem = 232448;
+  static constexpr int kStagesFit = (kMaxSmem - kFixed) / Geometry<KVDT>::kStageBytes;
+  static constexpr int kStages = kStagesFit < 32 ? kStagesFit : 32;
+  static constexpr int kStageRegion = kStages * Geometry<KVDT>::kStageBytes;
+  static constexpr int kBarOff = kStageRegion;                 // full[S], empty[S]
+  static constexpr int kMetaOff = kBarOff + 2 * 8 * kStages;   // int32 valid[S]
+  static constexpr int kAbortOff = kMetaOff + 4 * kStages;     // int32 abort flag
+  static constexpr int kMlOff = (kAbortOff + 4 + 15) & ~15;
+  static constexpr int kMergeOff = (kMlOff + kMlBytes + 15) & ~15;
+  static constexpr int kTotal = kMergeOff + kMergeBytes;
+  static constexpr int kDynamicBytes = kTotal + 1024;          // room to align the base
+  static_assert(kStages >= 4, "too few stages");
+  static_assert(kDynamicBytes <= kMaxSmem, "shared memory plan too large");
+};
+
+// Position of (row, dim) in the merge buffer: 32-dim chunks stay in place,
+// inside a chunk the float pairs rotate with the chunk index and the row so
+// that the consumers' fragment stores hit distinct banks.
+__device__ __forceinline__ int merge_pos(int row, int d) {
+  return row * 256 + (d & ~31) + (((d & 31) + 8 * ((d >> 5) & 3) + 2 * ((row & 7) >> 1)) & 31);
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp consumer state.
+
+template <int NTW>
+struct WarpState {
+  float o[16][NTW][4];  // O^T fragments: [m-tile of dims][n-tile of rows]
+  float m[NTW][2];      // running max (log2 domain) of the thread's 2 columns
+  float l[NTW][2];      // running partial sum of p (this thread's tokens)
+  int32_t lim[NTW][2];  // keys visible to each column (absolute count)
+
+  __device__ void reset() {
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+    }
+  }
+};
+
+// Query B-fragments of the warp's rows: for k-step kk the thread holds
+// (Q[row][64*tig + 4*kk + 0..1]) and (Q[row][64*tig + 4*kk + 2..3]), row =
+// 8*nt + gid of the warp's row block; fp16 for the NVFP4 path (the K tile is
+// fp16), bf16 bits for the bf16 path.
+template <int KVDT, int NTW>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, const Piece& pc, int row_base, int lane,
+                                       uint32_t (&qb)[NTW][16][2]) {
+  const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt) {
+    const int n = row_base + 8 * nt + gid;
+    const int rows = a.group * pc.s.qlen;
+    if (n < rows) {
+      const int t = pc.s.q0 + n / a.group;
+      const int hq = pc.h * a.group + n % a.group;
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(t) * a.hq + hq) * 256 +
+                                                        64 * tig);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = __ldg(src + c);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int word = 4 * c + e;  // dims 64*tig + 2*word, +1
+          uint32_t v = ws[e];
+          if (KVDT == PNKV_KV_NVFP4)
+            v = f32x2_to_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+          qb[nt][word >> 1][word & 1] = v;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) qb[nt][kk][0] = qb[nt][kk][1] = 0u;
+    }
+  }
+}
+
+// S^T (16 tokens x 8 rows per n-tile) for one page: NVFP4.
+template <int NTW>
+__device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const uint32_t (&qb)[NTW][16][2],
+                                         float (&s)[NTW][4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  // scales of blocks 4*tig .. 4*tig+3 for tokens gid and gid+8
+  const uint32_t sc_lo = lds32(sb + swz128(16, gid * 16 + 4 * tig));
+  const uint32_t sc_hi = lds32(sb + swz128(17, gid * 16 + 4 * tig));
+  const uint32_t slo01 = e4m3x2_to_f16x2(sc_lo & 0xFFFFu), slo23 = e4m3x2_to_f16x2(sc_lo >> 16);
+  const uint32_t shi01 = e4m3x2_to_f16x2(sc_hi & 0xFFFFu), shi23 = e4m3x2_to_f16x2(sc_hi >> 16);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // 16-byte chunk 2*tig + h: k-steps 8h .. 8h+7
+    const uint4 klo = lds128(sb + swz128(gid, 16 * (2 * tig + h)));
+    const uint4 khi = lds128(sb + swz128(gid + 8, 16 * (2 * tig + h)));
+    const uint32_t wl[4] = {klo.x, klo.y, klo.z, klo.w};
+    const uint32_t wh[4] = {khi.x, khi.y, khi.z, khi.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // word q: k-steps 8h + 2q, 8h + 2q + 1
+      const int blk = 2 * h + (q >> 1);  // block 4*tig + blk
+      const uint32_t sl = (blk < 2) ? slo01 : slo23;
+      const uint32_t sh = (blk < 2) ? shi01 : shi23;
+      const uint32_t sel = (blk & 1) ? 0x3232u : 0x1010u;
+      const uint32_t scl = prmt(sl, sl, sel), sch = prmt(sh, sh, sel);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int kk = 8 * h + 2 * q + half;
+        const uint32_t bl = wl[q] >> (16 * half), bh = wh[q] >> (16 * half);
+        uint32_t af[4];
+        af[0] = hmul2(e2m1x2_to_f16x2(bl & 0xFFu), scl);        // token gid, dims +0,+1
+        af[1] = hmul2(e2m1x2_to_f16x2(bh & 0xFFu), sch);        // token gid+8
+        af[2] = hmul2(e2m1x2_to_f16x2((bl >> 8) & 0xFFu), scl); // token gid, dims +2,+3
+        af[3] = hmul2(e2m1x2_to_f16x2((bh >> 8) & 0xFFu), sch);
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(s[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+      }
+    }
+  }
+}
+
+// S^T for one page: bf16 cache.
+template <int NTW>
+__device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const uint32_t (&qb)[NTW][16][2],
+                                        float (&s)[NTW][4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  const uint32_t rlo = 4 * gid + tig, rhi = 4 * (gid + 8) + tig;  // box rows
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // chunk c: words 4c..4c+3 -> k-steps 2c, 2c+1
+    const uint4 klo = lds128(sb + swz128(rlo, 16 * c));
+    const uint4 khi = lds128(sb + swz128(rhi, 16 * c));
+    {
+      const uint32_t af[4] = {klo.x, khi.x, klo.y, khi.y};
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) mma_bf16_16816(s[nt], af, qb[nt][2 * c][0], qb[nt][2 * c][1]);
+    }
+    {
+      const uint32_t af[4] = {klo.z, khi.z, klo.w, khi.w};
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt)
+        mma_bf16_16816(s[nt], af, qb[nt][2 * c + 1][0], qb[nt][2 * c + 1][1]);
+    }
+  }
+}
+
+// Online softmax on the page's logits; returns the P^T B-fragments.
+template <int NTW>
+__device__ __forceinline__ void softmax_page(WarpState<NTW>& st, float (&s)[NTW][4], float scale,
+                                             int32_t key0, int32_t page_lim, bool masked, int lane,
+                                             uint32_t (&pb)[NTW][2]) {
+  const int gid = lane >> 2;
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] *= scale;
+    if (masked) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = gid + ((e & 2) ? 8 : 0);
+        const int key = key0 + tok;
+        if (tok >= page_lim || key >= st.lim[nt][e & 1]) s[nt][e] = -INFINITY;
+      }
+    }
+    float mx0 = fmaxf(s[nt][0], s[nt][2]), mx1 = fmaxf(s[nt][1], s[nt][3]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(st.m[nt][0], mx0), mn1 = fmaxf(st.m[nt][1], mx1);
+    const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+    const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = fast_exp2(st.m[nt][0] - base0), al1 = fast_exp2(st.m[nt][1] - base1);
+    st.m[nt][0] = mn0;
+    st.m[nt][1] = mn1;
+    const uint32_t x0 = f32x2_to_f16x2(fast_exp2(s[nt][0] - base0), fast_exp2(s[nt][1] - base1));
+    const uint32_t x1 = f32x2_to_f16x2(fast_exp2(s[nt][2] - base0), fast_exp2(s[nt][3] - base1));
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x0));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x1));
+    st.l[nt][0] = st.l[nt][0] * al0 + (f0.x + f1.x);
+    st.l[nt][1] = st.l[nt][1] * al1 + (f0.y + f1.y);
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt) {
+      st.o[mt][nt][0] *= al0;
+      st.o[mt][nt][2] *= al0;
+      st.o[mt][nt][1] *= al1;
+      st.o[mt][nt][3] *= al1;
+    }
+    pb[nt][0] = movmatrix_trans(x0);
+    pb[nt][1] = movmatrix_trans(x1);
+  }
+}
+
+// O^T += V^T P^T for one page: NVFP4.
+template <int NTW>
+__device__ __forceinline__ void pv_nvfp4(uint32_t sb, int lane, WarpState<NTW>& st,
+                                         const uint32_t (&pb)[NTW][2], int page_lim) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int t0 = 2 * tig, t1 = 2 * tig + 1, t2 = 2 * tig + 8, t3 = 2 * tig + 9;
+  // scales of blocks 2*gid, 2*gid+1 for the four tokens (zero when masked)
+  auto vscale = [&](int t) -> uint32_t {
+    const uint32_t two = lds16(sb + swz128(34 + (t >> 3), (t & 7) * 16 + 2 * gid));
+    return t < page_lim ? e4m3x2_to_f16x2(two) : 0u;
+  };
+  const uint32_t s0 = vscale(t0), s1 = vscale(t1), s2 = vscale(t2), s3 = vscale(t3);
+  const uint4 v0 = lds128(sb + swz128(18 + t0, 16 * gid));
+  const uint4 v1 = lds128(sb + swz128(18 + t1, 16 * gid));
+  const uint4 v2 = lds128(sb + swz128(18 + t2, 16 * gid));
+  const uint4 v3 = lds128(sb + swz128(18 + t3, 16 * gid));
+  const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+  const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+  for (int mt = 0; mt < 16; ++mt) {
+    const uint32_t sel = (mt < 8) ? 0x1010u : 0x3232u;  // block 2*gid or 2*gid+1
+    const int wi = mt >> 2, sh = 8 * (mt & 3);
+    const uint32_t x = hmul2(e2m1x2_to_f16x2((w0[wi] >> sh) & 0xFFu), prmt(s0, s0, sel));
+    const uint32_t y = hmul2(e2m1x2_to_f16x2((w1[wi] >> sh) & 0xFFu), prmt(s1, s1, sel));
+    const uint32_t z = hmul2(e2m1x2_to_f16x2((w2[wi] >> sh) & 0xFFu), prmt(s2, s2, sel));
+    const uint32_t w = hmul2(e2m1x2_to_f16x2((w3[wi] >> sh) & 0xFFu), prmt(s3, s3, sel));
+    uint32_t af[4];
+    af[0] = prmt(x, y, 0x5410u);  // dim 32*gid + 2*mt,     tokens 2tig, 2tig+1
+    af[1] = prmt(x, y, 0x7632u);  // dim 32*gid + 2*mt + 1
+    af[2] = prmt(z, w, 0x5410u);  // tokens 2tig+8, 2tig+9
+    af[3] = prmt(z, w, 0x7632u);
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pb[nt][0], pb[nt][1]);
+  }
+}
+
+// O^T += V^T P^T for one page: bf16 cache (V widened to fp16).
+template <int NTW>
+__device__ __forceinline__ void pv_bf16(uint32_t sb, int lane, WarpState<NTW>& st,
+                                        const uint32_t (&pb)[NTW][2], int page_lim) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int toks[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // chunk c: words 16*gid + 4*c .. +3
+    uint32_t w[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = toks[k];
+      const uint4 v = lds128(sb + swz128(64 + 4 * t + (gid >> 1), 64 * (gid & 1) + 16 * c));
+      const bool ok = t < page_lim;
+      w[k][0] = ok ? v.x : 0u;
+      w[k][1] = ok ? v.y : 0u;
+      w[k][2] = ok ? v.z : 0u;
+      w[k][3] = ok ? v.w : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int mt = 4 * c + e;  // word 16*gid + mt of each token
+      uint32_t af[4];
+      af[0] = f32x2_to_f16x2(__uint_as_float(w[0][e] << 16), __uint_as_float(w[1][e] << 16));
+      af[1] = f32x2_to_f16x2(__uint_as_float(w[0][e] & 0xFFFF0000u), __uint_as_float(w[1][e] & 0xFFFF0000u));
+      af[2] = f32x2_to_f16x2(__uint_as_float(w[2][e] << 16), __uint_as_float(w[3][e] << 16));
+      af[3] = f32x2_to_f16x2(__uint_as_float(w[2][e] & 0xFFFF0000u), __uint_as_float(w[3][e] & 0xFFFF0000u));
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+
+template <int KVDT, int NTW, int RG>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
+  using P = Plan<KVDT, NTW, RG>;
+  using Geo = Geometry<KVDT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kBarOff);
+  uint64_t* empty = full + P::kStages;
+  int32_t* stage_valid = reinterpret_cast<int32_t*>(smem + P::kMetaOff);
+  volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + P::kAbortOff);
+  float* ml = reinterpret_cast<float*>(smem + P::kMlOff);
+  float* mbuf = reinterpret_cast<float*>(smem + P::kMergeOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], RG);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap);
+  __syncthreads();
+
+  // this CTA's unit range
+  const int64_t total = total_units(a, lane);
+  const int64_t chunk = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t u_begin = min(total, static_cast<int64_t>(blockIdx.x) * chunk);
+  const int64_t u_end = min(total, u_begin + chunk);
+
+  if (blockIdx.x == 0 && warp == 0) {
+    if (lane == 0) {
+      a.work_meta[0] = a.hkv;
+      a.work_meta[1] = a.group;
+      a.work_meta[2] = a.rows_per_slot;
+      a.work_meta[3] = a.batch;
+    }
+    // segments without units get an empty slot range here; every other
+    // segment's range is written by the CTA that holds its first unit
+    for (int b = lane; b < a.batch; b += 32)
+      if (load_seq(a, b, false).pages == 0)
+        for (int h = 0; h < a.hkv; ++h) {
+          a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h)] = 0;
+          a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h) + 1] = 0;
+        }
+  }
+
+  Walker walk;
+  walk.init(a, u_begin, u_end, lane);
+  Piece pc;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = l2_policy_evict_first();
+    int64_t issued = 0;
+    bool ok = true;
+    while (ok && walk.next(a, &pc)) {
+      const int32_t* row = a.page_table + static_cast<int64_t>(pc.b) * a.pt_stride + pc.p0;
+      for (int j0 = 0; j0 < pc.n && ok; j0 += 32) {
+        const int32_t my_page = (j0 + lane < pc.n) ? __ldg(row + j0 + lane) : 0;
+        const int cnt = min(32, pc.n - j0);
+        for (int j = 0; j < cnt; ++j) {
+          const int32_t page = __shfl_sync(0xffffffffu, my_page, j);
+          if (lane == 0) {
+            const int64_t i = issued;
+            const int s = static_cast<int>(i % P::kStages);
+            const uint32_t par = static_cast<uint32_t>((i / P::kStages) & 1) ^ 1u;
+            if (*abort_flag || !mbar_wait(&empty[s], par)) {
+              flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+            } else if (page < 0 || page >= a.num_pages) {
+              flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
+              stage_valid[s] = 0;
+              mbar_arrive(&full[s]);
+            } else {
+              stage_valid[s] = 1;
+              mbar_arrive_expect_tx(&full[s], Geo::kTxBytes);
+              const int32_t y = (page * a.hkv + pc.h) * Geo::kBoxRows;
+              tma_load_2d(smem + s * Geo::kStageBytes, &tmap, 0, y, &full[s], policy);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ++issued;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // drain: wait (bounded) for the loads that may still be in flight
+      const int64_t first = issued > P::kStages ? issued - P::kStages : 0;
+      for (int64_t i = first; i < issued; ++i)
+        mbar_wait(&full[i % P::kStages], static_cast<uint32_t>((i / P::kStages) & 1));
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  if (warp >= Consumers<RG>::kWarps) return;  // spare warp when RG does not divide 7
+  const int rg = warp % RG;
+  const int stream = warp / RG;
+  const int row_base = rg * 8 * NTW;
+  const int gid = lane >> 2, tig = lane & 3;
+  WarpState<NTW> st;
+  uint32_t qb[NTW][16][2];
+
+  while (walk.next(a, &pc)) {
+    const int rows = a.group * pc.s.qlen;
+    load_q<KVDT, NTW>(a, pc, row_base, lane, qb);
+    st.reset();
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int n = row_base + 8 * nt + 2 * tig + c;
+        st.lim[nt][c] = a.causal ? pc.s.len - pc.s.qlen + n / a.group + 1 : pc.s.len;
+      }
+    const int32_t mask_from = a.causal ? pc.s.len - pc.s.qlen + 1 : pc.s.len;  // first key some row cannot see
+    // units of this piece owned by this warp
+    int64_t i = pc.i0 + ((stream - pc.i0 % P::kStreams) % P::kStreams + P::kStreams) % P::kStreams;
+    for (; i < pc.i0 + pc.n; i += P::kStreams) {
+      const int s = static_cast<int>(i % P::kStages);
+      const uint32_t par = static_cast<uint32_t>((i / P::kStages) & 1);
+      if (*abort_flag || !mbar_wait(&full[s], par)) {
+        if (lane == 0) flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      if (stage_valid[s]) {
+        const int32_t page_idx = pc.p0 + static_cast<int32_t>(i - pc.i0);
+        const int32_t key0 = page_idx * 16;
+        const int32_t page_lim = pc.s.len - key0;           // valid tokens in the page
+        const bool masked = key0 + 16 > mask_from;
+        const uint32_t sb = smem_addr(smem + s * Geo::kStageBytes);
+        float sacc[NTW][4];
+        uint32_t pb[NTW][2];
+        if (KVDT == PNKV_KV_NVFP4) qk_nvfp4<NTW>(sb, lane, qb, sacc);
+        else qk_bf16<NTW>(sb, lane, qb, sacc);
+        softmax_page<NTW>(st, sacc, a.qk_scale_log2, key0, page_lim, masked, lane, pb);
+        if (KVDT == PNKV_KV_NVFP4) pv_nvfp4<NTW>(sb, lane, st, pb, page_lim);
+        else pv_bf16<NTW>(sb, lane, st, pb, page_lim);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- merge the warps' partial states (fixed order) and write the slot
+    // 1. full l per column; m is already uniform across the column's lanes
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float l = st.l[nt][c];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        st.l[nt][c] = l;
+        if (gid == 0) {
+          const int row = row_base + 8 * nt + 2 * tig + c;
+          ml[(stream * P::kRows + row) * 2 + 0] = st.m[nt][c];
+          ml[(stream * P::kRows + row) * 2 + 1] = l;
+        }
+      }
+    named_bar_sync(1, Consumers<RG>::kThreads);
+    // 2. this warp's weight per column: 2^(m_w - M)
+    float wgt[NTW][2];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int row = row_base + 8 * nt + 2 * tig + c;
+        float M = -INFINITY;
+        for (int k = 0; k < P::kStreams; ++k) M = fmaxf(M, ml[(k * P::kRows + row) * 2]);
+        wgt[nt][c] = (M == -INFINITY) ? 0.f : fast_exp2(st.m[nt][c] - M);
+      }
+    // 3. ordered accumulation into the merge buffer, one stream per round
+    for (int k = 0; k < P::kStreams; ++k) {
+      if (stream == k) {
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int row = row_base + 8 * nt + 2 * tig + c;
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+              const int d = 32 * gid + 2 * mt;
+              float2* dst = reinterpret_cast<float2*>(mbuf + merge_pos(row, d));
+              const float2 v = make_float2(st.o[mt][nt][c] * wgt[nt][c], st.o[mt][nt][c + 2] * wgt[nt][c]);
+              if (k == 0) {
+                *dst = v;
+              } else {
+                float2 acc = *dst;
+                acc.x += v.x;
+                acc.y += v.y;
+                *dst = acc;
+              }
+            }
+          }
+      }
+      named_bar_sync(1, Consumers<RG>::kThreads);
+    }
+    // 4. normalise and write the partial (all consumer threads, coalesced)
+    const int64_t slot = pc.b * static_cast<int64_t>(a.hkv) + pc.h + blockIdx.x;
+    const int nrows = min(rows, P::kRows);
+    for (int idx = threadIdx.x; idx < nrows * 64; idx += Consumers<RG>::kThreads) {
+      const int row = idx >> 6;
+      const int d4 = (idx & 63) * 4;
+      float M = -INFINITY;
+      for (int k = 0; k < P::kStreams; ++k) M = fmaxf(M, ml[(k * P::kRows + row) * 2]);
+      float L = 0.f;
+      if (M != -INFINITY)
+        for (int k = 0; k < P::kStreams; ++k)
+          L += ml[(k * P::kRows + row) * 2 + 1] * fast_exp2(ml[(k * P::kRows + row) * 2] - M);
+      const float inv = (L > 0.f) ? a.out_scale / L : 0.f;
+      float4 o;
+      o.x = mbuf[merge_pos(row, d4 + 0)] * inv;
+      o.y = mbuf[merge_pos(row, d4 + 1)] * inv;
+      o.z = mbuf[merge_pos(row, d4 + 2)] * inv;
+      o.w = mbuf[merge_pos(row, d4 + 3)] * inv;
+      if (slot < a.part_slots) {
+        reinterpret_cast<float4*>(a.o_part + (slot * a.rows_per_slot + row) * 256)[d4 >> 2] = o;
+        if (d4 == 0) a.lse_part[slot * a.rows_per_slot + row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+      }
+    }
+    // 5. the CTA holding the segment's first unit records where its slots are
+    if (threadIdx.x == 0 && pc.p0 == 0) {
+      const int64_t seg = pc.b * static_cast<int64_t>(a.hkv) + pc.h;
+      const int64_t first_cta = pc.seg_start / chunk;
+      const int64_t last_cta = (pc.seg_start + pc.s.pages - 1) / chunk;
+      a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg + first_cta);
+      a.work_meta[4 + 2 * seg + 1] = static_cast<int32_t>(last_cta - first_cta + 1);
+    }
+    named_bar_sync(1, Consumers<RG>::kThreads);
+    if (*abort_flag) break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// The pool seen as a 2-D byte tensor [num_pages * hkv * box_rows][128].
+int make_pool_map(const pnkv_cache* c, int box_rows, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return PNKV_ERR_CUDA;
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * box_rows;
+  if (rows >= (1ull << 31)) return PNKV_ERR_INVALID_ARG;  // TMA row coordinates are int32
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->pool, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PNKV_OK : PNKV_ERR_CUDA;
+}
+
+template <int KVDT, int NTW, int RG>
+int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
+  using P = Plan<KVDT, NTW, RG>;
+  auto kern = paged_decode_kernel<KVDT, NTW, RG>;
+  static bool configured = false;  // attribute set once per process (idempotent)
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kDynamicBytes) !=
+        cudaSuccess)
+      return PNKV_ERR_CUDA;
+    configured = true;
+  }
+  kern<<<grid, kThreads, P::kDynamicBytes, stream>>>(map, a);
+  return launch_status();
+}
+
+template <int KVDT>
+int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
+  const int rows = a.rows_per_slot;
+  if (rows <= 8) return launch_decode<KVDT, 1, 1>(map, a, grid, stream);
+  if (rows <= 16) return launch_decode<KVDT, 2, 1>(map, a, grid, stream);
+  if (rows <= 32) return launch_decode<KVDT, 2, 2>(map, a, grid, stream);
+  if (rows <= 64) return launch_decode<KVDT, 2, 4>(map, a, grid, stream);
+  return PNKV_ERR_UNSUPPORTED;
+}
+
+int decode_grid(int* grid) { return device_sm_count(grid); }
+
+}  // namespace
+}  // namespace pnkv
+
+extern "C" int64_t pnkv_decode_slots(const pnkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                     int32_t max_qlen) {
+  using namespace pnkv;
+  int st = check_cache(cache);
+  if (st != PNKV_OK) return st;
+  if (batch < 1 || max_qlen < 1 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
+    return PNKV_ERR_INVALID_ARG;
+  int grid = 0;
+  if ((st = decode_grid(&grid)) != PNKV_OK) return st;
+  return static_cast<int64_t>(batch) * cache->num_kv_heads + grid;
+}
+
+extern "C" int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads) {
+  if (batch < 1 || num_kv_heads < 1) return PNKV_ERR_INVALID_ARG;
+  return 4 + 2 * static_cast<int64_t>(batch) * num_kv_heads;
+}
+
+extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q_roped,
+                                      const int32_t* qo_indptr, const int32_t* page_table,
+                                      int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                                      int32_t num_q_heads, int32_t max_qlen, float sm_scale,
+                                      int32_t causal, float* o_part, float* lse_part, int64_t part_slots,
+                                      int32_t* work_meta, int32_t* dev_err, void* stream) {
+  using namespace pnkv;
+  int st = check_cache(cache);
+  if (st != PNKV_OK) return st;
+  if (!q_roped || !qo_indptr || !page_table || !seq_lens || !o_part || !lse_part || !work_meta || !dev_err)
+    return PNKV_ERR_INVALID_ARG;
+  if (batch < 1 || pt_stride < 1 || max_qlen < 1 || max_qlen > 8192 || num_q_heads < 1 ||
+      num_q_heads % cache->num_kv_heads != 0)
+    return PNKV_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return PNKV_ERR_INVALID_ARG;
+  if (!aligned(q_roped, 16) || !aligned(o_part, 16) || !aligned(lse_part, 4)) return PNKV_ERR_INVALID_ARG;
+  const int group = num_q_heads / cache->num_kv_heads;
+  if (group > 8) return PNKV_ERR_UNSUPPORTED;
+  const int64_t rows_per_slot = static_cast<int64_t>(group) * max_qlen;
+  int grid = 0;
+  if ((st = decode_grid(&grid)) != PNKV_OK) return st;
+  if (part_slots < static_cast<int64_t>(batch) * cache->num_kv_heads + grid) return PNKV_ERR_INVALID_ARG;
+  if (rows_per_slot > 64) return PNKV_ERR_UNSUPPORTED;
+
+  DecodeArgs a;
+  a.num_pages = cache->num_pages;
+  a.hkv = cache->num_kv_heads;
+  a.group = group;
+  const float kscale = cache->dtype == PNKV_KV_NVFP4 ? cache->k_scale : 1.0f;
+  a.qk_scale_log2 = sm_scale * kscale * kLog2e;
+  a.out_scale = cache->dtype == PNKV_KV_NVFP4 ? cache->v_scale : 1.0f;
+  a.q = q_roped;
+  a.qo_indptr = qo_indptr;
+  a.page_table = page_table;
+  a.pt_stride = pt_stride;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.hq = num_q_heads;
+  a.max_qlen = max_qlen;
+  a.rows_per_slot = static_cast<int32_t>(rows_per_slot);
+  a.causal = causal ? 1 : 0;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.part_slots = part_slots;
+  a.work_meta = work_meta;
+  a.dev_err = dev_err;
+
+  CUtensorMap map;
+  const int box_rows = cache->dtype == PNKV_KV_NVFP4 ? Geometry<PNKV_KV_NVFP4>::kBoxRows
+                                                     : Geometry<PNKV_KV_BF16>::kBoxRows;
+  if ((st = make_pool_map(cache, box_rows, &map)) != PNKV_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  if (cache->dtype == PNKV_KV_NVFP4) return dispatch_rows<PNKV_KV_NVFP4>(map, a, grid, s);
+  return dispatch_rows<PNKV_KV_BF16>(map, a, grid, s);
+}

@@ -1,0 +1,47 @@
+// Host-side helpers shared by the libpnkv entry points: argument checks,
+// launch-error mapping and the per-device SM count.
+#pragma once
+
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pnkv.h"
+
+namespace pnkv {
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Status of the most recent launch on this thread.
+inline int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? PNKV_OK : PNKV_ERR_CUDA;
+}
+
+// SM count of the current device (cached per device id).
+int device_sm_count(int* out_sms);
+
+// Pool geometry checks shared by every call that touches the pool.
+inline int check_cache(const pnkv_cache* c) {
+  if (!c || !c->pool || c->num_pages <= 0 || c->page_size != 16 || c->head_dim != 256 ||
+      c->num_kv_heads < 1 || c->num_kv_heads > 16)
+    return PNKV_ERR_INVALID_ARG;
+  if (c->dtype != PNKV_KV_BF16 && c->dtype != PNKV_KV_NVFP4) return PNKV_ERR_INVALID_ARG;
+  if (!aligned(c->pool, 128)) return PNKV_ERR_INVALID_ARG;
+  if (c->dtype == PNKV_KV_NVFP4) {
+    if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || !std::isfinite(c->k_scale) ||
+        !std::isfinite(c->v_scale))
+      return PNKV_ERR_INVALID_ARG;
+  }
+  return PNKV_OK;
+}
+
+// Bytes of one KV head's record inside a page (head_dim 256, 16 slots).
+inline int64_t head_record_bytes(int dtype) {
+  return dtype == PNKV_KV_NVFP4 ? 2 * 16 * (128 + 16) : 2 * 16 * 256 * 2;
+}
+
+}  // namespace pnkv

@@ -46,6 +46,7 @@ namespace {
 // One warp produces; the consumers are the largest multiple of RG below 8.
 constexpr int kThreads = 256;
 constexpr int kProducerWarp = 7;
+constexpr int kIssueLanes = 8;  // producer lanes that issue TMA loads together
 template <int RG>
 struct Consumers {
   static constexpr int kWarps = (7 / RG) * RG;
@@ -313,13 +314,18 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, const Piece& pc, int
   }
 }
 
-// S^T (16 tokens x 8 rows per n-tile) for one page: NVFP4.
+// S^T (16 tokens x 8 rows per n-tile) for one page: NVFP4.  The 16 k-steps
+// feed four independent accumulator sets (k-step mod 4) so that consecutive
+// MMAs do not wait on each other; the sets are summed at the end.
 template <int NTW>
 __device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const uint32_t (&qb)[NTW][16][2],
                                          float (&s)[NTW][4]) {
   const int gid = lane >> 2, tig = lane & 3;
+  float acc[4][NTW][4];
 #pragma unroll
-  for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
   // scales of blocks 4*tig .. 4*tig+3 for tokens gid and gid+8
   const uint32_t sc_lo = lds32(sb + swz128(16, gid * 16 + 4 * tig));
   const uint32_t sc_hi = lds32(sb + swz128(17, gid * 16 + 4 * tig));
@@ -339,28 +345,37 @@ __device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const uint32_t (
       const uint32_t sel = (blk & 1) ? 0x3232u : 0x1010u;
       const uint32_t scl = prmt(sl, sl, sel), sch = prmt(sh, sh, sel);
 #pragma unroll
+      uint32_t cl[4], ch[4];
+      e2m1x8_unpack(wl[q], cl);
+      e2m1x8_unpack(wh[q], ch);
       for (int half = 0; half < 2; ++half) {
         const int kk = 8 * h + 2 * q + half;
-        const uint32_t bl = wl[q] >> (16 * half), bh = wh[q] >> (16 * half);
         uint32_t af[4];
-        af[0] = hmul2(e2m1x2_to_f16x2(bl & 0xFFu), scl);        // token gid, dims +0,+1
-        af[1] = hmul2(e2m1x2_to_f16x2(bh & 0xFFu), sch);        // token gid+8
-        af[2] = hmul2(e2m1x2_to_f16x2((bl >> 8) & 0xFFu), scl); // token gid, dims +2,+3
-        af[3] = hmul2(e2m1x2_to_f16x2((bh >> 8) & 0xFFu), sch);
+        af[0] = hmul2(cl[2 * half], scl);
+        af[1] = hmul2(ch[2 * half], sch);
+        af[2] = hmul2(cl[2 * half + 1], scl);
+        af[3] = hmul2(ch[2 * half + 1], sch);
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(s[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+        for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(acc[kk & 3][nt], af, qb[nt][kk][0], qb[nt][kk][1]);
       }
     }
   }
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = (acc[0][nt][e] + acc[1][nt][e]) + (acc[2][nt][e] + acc[3][nt][e]);
 }
 
-// S^T for one page: bf16 cache.
+// S^T for one page: bf16 cache (four independent accumulator sets, as above).
 template <int NTW>
 __device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const uint32_t (&qb)[NTW][16][2],
                                         float (&s)[NTW][4]) {
   const int gid = lane >> 2, tig = lane & 3;
+  float acc[4][NTW][4];
 #pragma unroll
-  for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
   const uint32_t rlo = 4 * gid + tig, rhi = 4 * (gid + 8) + tig;  // box rows
 #pragma unroll
   for (int c = 0; c < 8; ++c) {  // chunk c: words 4c..4c+3 -> k-steps 2c, 2c+1
@@ -369,15 +384,20 @@ __device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const uint32_t (&
     {
       const uint32_t af[4] = {klo.x, khi.x, klo.y, khi.y};
 #pragma unroll
-      for (int nt = 0; nt < NTW; ++nt) mma_bf16_16816(s[nt], af, qb[nt][2 * c][0], qb[nt][2 * c][1]);
+      for (int nt = 0; nt < NTW; ++nt)
+        mma_bf16_16816(acc[(2 * c) & 3][nt], af, qb[nt][2 * c][0], qb[nt][2 * c][1]);
     }
     {
       const uint32_t af[4] = {klo.z, khi.z, klo.w, khi.w};
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt)
-        mma_bf16_16816(s[nt], af, qb[nt][2 * c + 1][0], qb[nt][2 * c + 1][1]);
+        mma_bf16_16816(acc[(2 * c + 1) & 3][nt], af, qb[nt][2 * c + 1][0], qb[nt][2 * c + 1][1]);
     }
   }
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = (acc[0][nt][e] + acc[1][nt][e]) + (acc[2][nt][e] + acc[3][nt][e]);
 }
 
 // Online softmax on the page's logits; returns the P^T B-fragments.
@@ -416,12 +436,15 @@ __device__ __forceinline__ void softmax_page(WarpState<NTW>& st, float (&s)[NTW]
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x1));
     st.l[nt][0] = st.l[nt][0] * al0 + (f0.x + f1.x);
     st.l[nt][1] = st.l[nt][1] * al1 + (f0.y + f1.y);
+    // rescale the accumulators only when some column's running max moved
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-    for (int mt = 0; mt < 16; ++mt) {
-      st.o[mt][nt][0] *= al0;
-      st.o[mt][nt][2] *= al0;
-      st.o[mt][nt][1] *= al1;
-      st.o[mt][nt][3] *= al1;
+      for (int mt = 0; mt < 16; ++mt) {
+        st.o[mt][nt][0] *= al0;
+        st.o[mt][nt][2] *= al0;
+        st.o[mt][nt][1] *= al1;
+        st.o[mt][nt][3] *= al1;
+      }
     }
     pb[nt][0] = movmatrix_trans(x0);
     pb[nt][1] = movmatrix_trans(x1);
@@ -446,14 +469,21 @@ __device__ __forceinline__ void pv_nvfp4(uint32_t sb, int lane, WarpState<NTW>& 
   const uint4 v3 = lds128(sb + swz128(18 + t3, 16 * gid));
   const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
   const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+  uint32_t c0[4], c1[4], c2[4], c3[4];
 #pragma unroll
   for (int mt = 0; mt < 16; ++mt) {
     const uint32_t sel = (mt < 8) ? 0x1010u : 0x3232u;  // block 2*gid or 2*gid+1
-    const int wi = mt >> 2, sh = 8 * (mt & 3);
-    const uint32_t x = hmul2(e2m1x2_to_f16x2((w0[wi] >> sh) & 0xFFu), prmt(s0, s0, sel));
-    const uint32_t y = hmul2(e2m1x2_to_f16x2((w1[wi] >> sh) & 0xFFu), prmt(s1, s1, sel));
-    const uint32_t z = hmul2(e2m1x2_to_f16x2((w2[wi] >> sh) & 0xFFu), prmt(s2, s2, sel));
-    const uint32_t w = hmul2(e2m1x2_to_f16x2((w3[wi] >> sh) & 0xFFu), prmt(s3, s3, sel));
+    const int wi = mt >> 2, bi = mt & 3;
+    if (bi == 0) {
+      e2m1x8_unpack(w0[wi], c0);
+      e2m1x8_unpack(w1[wi], c1);
+      e2m1x8_unpack(w2[wi], c2);
+      e2m1x8_unpack(w3[wi], c3);
+    }
+    const uint32_t x = hmul2(c0[bi], prmt(s0, s0, sel));
+    const uint32_t y = hmul2(c1[bi], prmt(s1, s1, sel));
+    const uint32_t z = hmul2(c2[bi], prmt(s2, s2, sel));
+    const uint32_t w = hmul2(c3[bi], prmt(s3, s3, sel));
     uint32_t af[4];
     af[0] = prmt(x, y, 0x5410u);  // dim 32*gid + 2*mt,     tokens 2tig, 2tig+1
     af[1] = prmt(x, y, 0x7632u);  // dim 32*gid + 2*mt + 1
@@ -562,18 +592,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && walk.next(a, &pc)) {
       const int32_t* row = a.page_table + static_cast<int64_t>(pc.b) * a.pt_stride + pc.p0;
       for (int j0 = 0; j0 < pc.n && ok; j0 += 32) {
-        const int32_t my_page = (j0 + lane < pc.n) ? __ldg(row + j0 + lane) : 0;
-        const int cnt = min(32, pc.n - j0);
-        for (int j = 0; j < cnt; ++j) {
-          const int32_t page = __shfl_sync(0xffffffffu, my_page, j);
-          if (lane == 0) {
-            const int64_t i = issued;
+        // lane j handles unit j0 + j: its own page id, stage and barrier;
+        // lanes issue in groups of kIssueLanes so the ring refills steadily
+        const bool mine = j0 + lane < pc.n;
+        const int32_t page = mine ? __ldg(row + j0 + lane) : 0;
+        bool lane_ok = true;
+#pragma unroll 1
+        for (int g = 0; g < 32 / kIssueLanes; ++g) {
+          if (mine && lane / kIssueLanes == g) {
+            const int64_t i = issued + lane;
             const int s = static_cast<int>(i % P::kStages);
             const uint32_t par = static_cast<uint32_t>((i / P::kStages) & 1) ^ 1u;
             if (*abort_flag || !mbar_wait(&empty[s], par)) {
-              flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
-              *abort_flag = 1;
-              ok = false;
+              lane_ok = false;
             } else if (page < 0 || page >= a.num_pages) {
               flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
               stage_valid[s] = 0;
@@ -585,9 +616,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(smem + s * Geo::kStageBytes, &tmap, 0, y, &full[s], policy);
             }
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          ++issued;
+          __syncwarp();
         }
+        if (!__all_sync(0xffffffffu, lane_ok)) {
+          if (lane == 0) {
+            flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          ok = false;
+        }
+        issued += min(32, pc.n - j0);
       }
     }
     if (!ok && lane == 0) {

@@ -26,7 +26,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // A pipeline wait gives up after this long (the GPU is shared and may be
 // time-sliced, so the bound is generous); the kernel then flags
 // PNKV_DEV_ERR_TIMEOUT and winds down instead of hanging.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // -------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -218,4 +218,13 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t byte) {
   return row * 128u + ((((byte >> 4) ^ row) & 7u) << 4) + (byte & 15u);
 }
 
+
+// Eight E2M1 codes (one 32-bit word, element 2k in the low nibble of byte k)
+// -> four f16x2 values, o[k] = (element 2k, element 2k+1) of byte k.  Exact.
+__device__ __forceinline__ void e2m1x8_unpack(uint32_t w, uint32_t (&o)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+      " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
 }  // namespace pnkv

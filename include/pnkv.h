@@ -248,6 +248,43 @@ int split_kv_combine(const float* o_part, const float* lse_part,
                      void* out, int32_t out_is_fp32, float* lse_out,
                      void* stream);
 
+/* Bytes of the fixed device scratch behind paged_decode_attention_noalloc. */
+#define PNKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* paged_decode_attention followed by split_kv_combine, allocating nothing.
+ * (No counterpart in the pages: this is a convenience of this library.)
+ *
+ * For callers that cannot allocate device memory for the split-KV partials:
+ * an engine whose device memory is all reserved up front by its own
+ * allocator and that does not let libraries call cudaMalloc, a
+ * latency-critical loop in which cudaMalloc could synchronise the device,
+ * or C code with no tensor library at hand.  The partials live instead in a
+ * fixed scratch array of PNKV_NOALLOC_SCRATCH_BYTES (8 MiB) inside the
+ * library's own device memory; every GPU that loads the library holds it
+ * until the process exits.  The caller passes only inputs and outputs.
+ *   - Arguments and results are those of paged_decode_attention and
+ *     split_kv_combine (total_q = qo_indptr[batch], host copy; out bf16, or
+ *     fp32 when out_is_fp32; lse_out may be NULL).
+ *   - Requests whose partials do not fit the scratch -- (batch * num_kv_heads
+ *     + SM count) slots of num_q_heads / num_kv_heads * max_qlen rows of
+ *     257 floats, plus the work metadata -- return PNKV_ERR_INVALID_ARG
+ *     before anything is launched.
+ *   - The first call on a device looks up the scratch's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - No scratch content needs to start at zero: each call writes every
+ *     metadata entry and partial that its own combine reads.
+ *   - All calls share the one scratch: calls that overlap on the GPU (on
+ *     different streams, or from several threads) race and corrupt each
+ *     other's results; serialise them.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine. */
+int paged_decode_attention_noalloc(const pnkv_cache* cache, const uint16_t* q_roped,
+                                   const int32_t* qo_indptr, const int32_t* page_table,
+                                   int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                                   int32_t num_q_heads, int32_t max_qlen, float sm_scale,
+                                   int32_t causal, int64_t total_q, void* out,
+                                   int32_t out_is_fp32, float* lse_out, int32_t* dev_err,
+                                   void* stream);
+
 /* Static text for a status code. */
 const char* pnkv_status_string(int status);
 

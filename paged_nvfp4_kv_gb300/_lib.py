@@ -53,6 +53,9 @@ SIGNATURES = [
       _P, _P, _P]),
     ("split_kv_combine", ctypes.c_int,
      [_P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _I32, _P, _P]),
+    ("paged_decode_attention_noalloc", ctypes.c_int,
+     [ctypes.POINTER(CacheDesc), _P, _P, _P, _I64, _P, _I32, _I32, _I32, _F, _I32, _I64, _P, _I32,
+      _P, _P, _P]),
     ("pnkv_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("pnkv_version", ctypes.c_int, []),
 ]

@@ -41,15 +41,15 @@
 namespace pnkv {
 namespace {
 
-// A CTA is one warpgroup pair (8 warps, 256 threads): register allocation
-// is per 4-warp group, so 8 warps keep the full 255 registers per thread.
-// One warp produces; the consumers are the largest multiple of RG below 8.
-constexpr int kThreads = 256;
-constexpr int kProducerWarp = 7;
+// A CTA has NW warps: the last one produces, the consumers are the largest
+// multiple of RG below it.  Register allocation is per 4-warp group, so 8
+// warps (256 threads) keep 255 registers per thread and 12 warps (384) keep
+// 168: the single-n-tile path fits 168 and runs 11 consumers, the two-n-tile
+// paths need the larger budget and run with 8 warps.
 constexpr int kIssueLanes = 8;  // producer lanes that issue TMA loads together
-template <int RG>
+template <int NW, int RG>
 struct Consumers {
-  static constexpr int kWarps = (7 / RG) * RG;
+  static constexpr int kWarps = ((NW - 1) / RG) * RG;
   static constexpr int kThreads = kWarps * 32;
 };
 constexpr float kLog2e = 1.4426950408889634f;
@@ -223,9 +223,9 @@ struct Walker {
 // ---------------------------------------------------------------------------
 // Shared memory plan.
 
-template <int KVDT, int NTW, int RG>
+template <int KVDT, int NTW, int RG, int NW>
 struct Plan {
-  static constexpr int kStreams = Consumers<RG>::kWarps / RG;   // warps that split the units
+  static constexpr int kStreams = Consumers<NW, RG>::kWarps / RG;   // warps that split the units
   static constexpr int kRows = 8 * NTW * RG;             // query rows per KV head handled
   static constexpr int kMergeBytes = kRows * 256 * 4;
   static constexpr int kMlBytes = kStreams * kRows * 2 * 4;
@@ -529,10 +529,12 @@ __device__ __forceinline__ void pv_bf16(uint32_t sb, int lane, WarpState<NTW>& s
 
 // ---------------------------------------------------------------------------
 
-template <int KVDT, int NTW, int RG>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KVDT, int NTW, int RG, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
-  using P = Plan<KVDT, NTW, RG>;
+  using P = Plan<KVDT, NTW, RG, NW>;
+  using C = Consumers<NW, RG>;
+  constexpr int kProducerWarp = NW - 1;
   using Geo = Geometry<KVDT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -638,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  if (warp >= Consumers<RG>::kWarps) return;  // spare warp when RG does not divide 7
+  if (warp >= C::kWarps) return;  // spare warp when RG does not divide 7
   const int rg = warp % RG;
   const int stream = warp / RG;
   const int row_base = rg * 8 * NTW;
@@ -703,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ml[(stream * P::kRows + row) * 2 + 1] = l;
         }
       }
-    named_bar_sync(1, Consumers<RG>::kThreads);
+    named_bar_sync(1, C::kThreads);
     // 2. this warp's weight per column: 2^(m_w - M)
     float wgt[NTW][2];
 #pragma unroll
@@ -739,12 +741,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
       }
-      named_bar_sync(1, Consumers<RG>::kThreads);
+      named_bar_sync(1, C::kThreads);
     }
     // 4. normalise and write the partial (all consumer threads, coalesced)
     const int64_t slot = pc.b * static_cast<int64_t>(a.hkv) + pc.h + blockIdx.x;
     const int nrows = min(rows, P::kRows);
-    for (int idx = threadIdx.x; idx < nrows * 64; idx += Consumers<RG>::kThreads) {
+    for (int idx = threadIdx.x; idx < nrows * 64; idx += C::kThreads) {
       const int row = idx >> 6;
       const int d4 = (idx & 63) * 4;
       float M = -INFINITY;
@@ -772,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg + first_cta);
       a.work_meta[4 + 2 * seg + 1] = static_cast<int32_t>(last_cta - first_cta + 1);
     }
-    named_bar_sync(1, Consumers<RG>::kThreads);
+    named_bar_sync(1, C::kThreads);
     if (*abort_flag) break;
   }
 }
@@ -809,10 +811,10 @@ int make_pool_map(const pnkv_cache* c, int box_rows, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? PNKV_OK : PNKV_ERR_CUDA;
 }
 
-template <int KVDT, int NTW, int RG>
+template <int KVDT, int NTW, int RG, int NW>
 int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
-  using P = Plan<KVDT, NTW, RG>;
-  auto kern = paged_decode_kernel<KVDT, NTW, RG>;
+  using P = Plan<KVDT, NTW, RG, NW>;
+  auto kern = paged_decode_kernel<KVDT, NTW, RG, NW>;
   static bool configured = false;  // attribute set once per process (idempotent)
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kDynamicBytes) !=
@@ -820,17 +822,17 @@ int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
       return PNKV_ERR_CUDA;
     configured = true;
   }
-  kern<<<grid, kThreads, P::kDynamicBytes, stream>>>(map, a);
+  kern<<<grid, NW * 32, P::kDynamicBytes, stream>>>(map, a);
   return launch_status();
 }
 
 template <int KVDT>
 int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
   const int rows = a.rows_per_slot;
-  if (rows <= 8) return launch_decode<KVDT, 1, 1>(map, a, grid, stream);
-  if (rows <= 16) return launch_decode<KVDT, 2, 1>(map, a, grid, stream);
-  if (rows <= 32) return launch_decode<KVDT, 2, 2>(map, a, grid, stream);
-  if (rows <= 64) return launch_decode<KVDT, 2, 4>(map, a, grid, stream);
+  if (rows <= 8) return launch_decode<KVDT, 1, 1, 12>(map, a, grid, stream);
+  if (rows <= 16) return launch_decode<KVDT, 2, 1, 8>(map, a, grid, stream);
+  if (rows <= 32) return launch_decode<KVDT, 2, 2, 8>(map, a, grid, stream);
+  if (rows <= 64) return launch_decode<KVDT, 2, 4, 8>(map, a, grid, stream);
   return PNKV_ERR_UNSUPPORTED;
 }
 

@@ -42,10 +42,10 @@ namespace pnkv {
 namespace {
 
 // A CTA has NW warps: the last one produces, the consumers are the largest
-// multiple of RG below it.  Register allocation is per 4-warp group, so 8
-// warps (256 threads) keep 255 registers per thread and 12 warps (384) keep
-// 168: the single-n-tile path fits 168 and runs 11 consumers, the two-n-tile
-// paths need the larger budget and run with 8 warps.
+// multiple of RG below it.  Register allocation is per 4-warp group, so up
+// to 8 warps (256 threads) keep 255 registers per thread and 12 warps (384)
+// keep 168: the single-n-tile NVFP4 path fits 168 and runs 11 consumers; the
+// other paths need the larger budget and run with at most 8 warps.
 constexpr int kIssueLanes = 8;  // producer lanes that issue TMA loads together
 template <int NW, int RG>
 struct Consumers {
@@ -223,6 +223,11 @@ struct Walker {
 // ---------------------------------------------------------------------------
 // Shared memory plan.
 
+// The stage count is a multiple of the number of consumer streams, so unit
+// i always lands in a stage that only stream i % kStreams reads: a consumer
+// then waits on a stage whose previous round it consumed itself, i.e. never
+// more than one barrier phase ahead (a parity wait cannot tell phase k from
+// phase k + 2, so a wait two phases ahead would pass on stale data).
 template <int KVDT, int NTW, int RG, int NW>
 struct Plan {
   static constexpr int kStreams = Consumers<NW, RG>::kWarps / RG;   // warps that split the units
@@ -232,7 +237,8 @@ struct Plan {
   static constexpr int kFixed = kMergeBytes + kMlBytes + 1024 /*align*/ + 1024 /*bars, flags*/;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kStagesFit = (kMaxSmem - kFixed) / Geometry<KVDT>::kStageBytes;
-  static constexpr int kStages = kStagesFit < 32 ? kStagesFit : 32;
+  static constexpr int kStagesCap = kStagesFit < 48 ? kStagesFit : 48;
+  static constexpr int kStages = (kStagesCap / kStreams) * kStreams;
   static constexpr int kStageRegion = kStages * Geometry<KVDT>::kStageBytes;
   static constexpr int kBarOff = kStageRegion;                 // full[S], empty[S]
   static constexpr int kMetaOff = kBarOff + 2 * 8 * kStages;   // int32 valid[S]
@@ -241,7 +247,9 @@ struct Plan {
   static constexpr int kMergeOff = (kMlOff + kMlBytes + 15) & ~15;
   static constexpr int kTotal = kMergeOff + kMergeBytes;
   static constexpr int kDynamicBytes = kTotal + 1024;          // room to align the base
-  static_assert(kStages >= 4, "too few stages");
+  static_assert(kStages >= 2 * kStreams, "every consumer stream needs two stages");
+  static_assert(kStages % kStreams == 0, "stages must split evenly over the streams");
+  static_assert(kStages >= kIssueLanes, "lanes that issue together need distinct stages");
   static_assert(kDynamicBytes <= kMaxSmem, "shared memory plan too large");
 };
 
@@ -829,10 +837,14 @@ int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
 template <int KVDT>
 int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
   const int rows = a.rows_per_slot;
-  if (rows <= 8) return launch_decode<KVDT, 1, 1, 12>(map, a, grid, stream);
-  if (rows <= 16) return launch_decode<KVDT, 2, 1, 8>(map, a, grid, stream);
-  if (rows <= 32) return launch_decode<KVDT, 2, 2, 8>(map, a, grid, stream);
-  if (rows <= 64) return launch_decode<KVDT, 2, 4, 8>(map, a, grid, stream);
+  // warps per CTA: NVFP4 stages are small, so many consumer streams each keep
+  // two or more stages; bf16 stages are 16 KiB, so fewer streams share the
+  // 13 that fit and each still double-buffers.
+  constexpr bool fp4 = KVDT == PNKV_KV_NVFP4;
+  if (rows <= 8) return launch_decode<KVDT, 1, 1, fp4 ? 12 : 7>(map, a, grid, stream);
+  if (rows <= 16) return launch_decode<KVDT, 2, 1, 7>(map, a, grid, stream);
+  if (rows <= 32) return launch_decode<KVDT, 2, 2, 7>(map, a, grid, stream);
+  if (rows <= 64) return launch_decode<KVDT, 2, 4, 5>(map, a, grid, stream);
   return PNKV_ERR_UNSUPPORTED;
 }
 

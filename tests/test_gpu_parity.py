@@ -1,9 +1,11 @@
 """GPU parity of the whole decode path against the CPU oracle, stage by stage
 on identical inputs:
 
-  1. YaRN table: GPU vs oracle, at most 1 fp32 ulp apart, mismatches rare
-     (both evaluate cos/sin of a double angle; libraries may differ in the
-     last double bit, which flips a binary32 rounding now and then).
+  1. YaRN table: GPU vs oracle within 2^-22 absolute, mismatching entries
+     rare.  Both sides evaluate pow/cos/sin in double; the libraries may
+     differ in the last double bit of an inverse frequency, which the
+     position multiplies (p * 2^-52 relative) -- harmless in absolute terms
+     but worth a few binary32 ulps where cos/sin is near zero.
   2. Roped queries and keys: bit-exact given the GPU table.
   3. Pool bytes (E2M1 codes, E4M3 scales, page placement; bf16 values):
      bit-exact given the GPU table.
@@ -57,6 +59,11 @@ CASES = {
     "qlen8-nvfp4": ("nvfp4", [300, 1800], [8, 3]),
     "qlen8-bf16": ("bf16", [300, 1800], [8, 3]),
     "page-edge-nvfp4": ("nvfp4", [16, 15, 17, 31, 32, 0], [1, 1, 1, 1, 1, 1]),
+    # long sequences: every CTA takes many units and wraps its stage ring
+    "long-bf16": ("bf16", [65535], [1]),
+    "long-nvfp4": ("nvfp4", [70000, 7000], [1, 1]),
+    "long-verify5-nvfp4": ("nvfp4", [40000, 23000], [5, 5]),
+    "long-verify5-bf16": ("bf16", [30000], [5]),
 }
 
 
@@ -72,11 +79,10 @@ def test_table_close_to_oracle(run):
     w, s, *_ = run
     cos_o, sin_o = oracle_path.tables(w, s.max_pos)
     for got, want in ((s.cos, cos_o), (s.sin, sin_o)):
-        g = got.cpu().numpy().view(np.int32).astype(np.int64)
-        o = np.asarray(want, dtype=np.float32).view(np.int32).astype(np.int64)
-        ulps = np.abs(g - o)
-        assert ulps.max() <= 1
-        assert (ulps > 0).mean() < 1e-3
+        g = got.cpu().numpy().astype(np.float64)
+        d = np.abs(g - want)
+        assert d.max() <= 2.0 ** -22, d.max()
+        assert (d > 0).mean() < 1e-2, (d > 0).mean()
 
 
 def test_roped_q_bit_exact(run):

@@ -106,7 +106,8 @@ typedef struct {
  *   NVFP4, head_dim 256 (4,608 bytes):
  *     K codes  [16 slots][128 B]  element 2k in the low nibble of byte k
  *     K scales [16 slots][16 B]   E4M3, one per 16 contiguous elements
- *     V codes  [16 slots][128 B]
+ *     V codes  [8 slot pairs][256 B]  byte d of pair i: element d of slot 2i
+ *                                  in the low nibble, of slot 2i+1 in the high
  *     V scales [16 slots][16 B]
  *   bf16, head_dim 256 (16,384 bytes):
  *     K [16 slots][256] bf16, then V [16 slots][256] bf16

@@ -2,8 +2,8 @@
 Test infrastructure only (see ``oracle/__init__.py``).
 
 The pages describe the pool only as fixed-size blocks in one shared pool
-sized at start-up and not divided among request lanes ("ninfer-windows-tp2"
-README, section "Current limits"), with a head-major ("HND") layout inside a
+sized at start-up and not divided among request lanes ("NInfer -- Windows 11 TP2
+fork" README, section "Limitations"), with a head-major ("HND") layout inside a
 block ("262,144 Tokens on One RTX 5090 ...", section "The stack, for the
 impatient").  The byte layout below is this library's own choice; it is the
 definition the GPU encoder is checked against, byte for byte.
@@ -15,8 +15,13 @@ Inside a page the record of each KV head h is contiguous, heads in order:
   NVFP4 (4,608 bytes per page-head, D = 256):
     K codes   [16 slots][D/2 bytes]   element 2k in the low nibble of byte k
     K scales  [16 slots][D/16 bytes]  E4M3, one per 16 contiguous elements
-    V codes   [16 slots][D/2 bytes]
+    V codes   [8 slot pairs][D bytes] byte d of pair i: element d of slot
+                                      2i in the low nibble, of slot 2i+1 in
+                                      the high nibble
     V scales  [16 slots][D/16 bytes]
+  (V pairs slots rather than elements because the P.V product reduces over
+  tokens: one byte then widens to the two consecutive-token values a
+  tensor-core operand register holds.)
   bf16 (16,384 bytes per page-head):
     K [16 slots][D] bf16 (little-endian), then V [16 slots][D] bf16
 """
@@ -41,14 +46,15 @@ def page_bytes(dtype, num_kv_heads, head_dim):
 
 
 def _sections(dtype, head_dim):
-    """(offset, row_bytes) of K-data, K-scale, V-data, V-scale sections."""
+    """(offset, row_bytes) of K-data, K-scale, V-data, V-scale sections.
+    For NVFP4 the V-data "row" is a slot pair (head_dim bytes)."""
     if dtype == NVFP4:
         cb, sb = head_dim // 2, head_dim // 16
         k0 = 0
         ks = k0 + PAGE * cb
         v0 = ks + PAGE * sb
         vs = v0 + PAGE * cb
-        return (k0, cb), (ks, sb), (v0, cb), (vs, sb)
+        return (k0, cb), (ks, sb), (v0, head_dim), (vs, sb)
     rb = head_dim * 2
     return (0, rb), None, (PAGE * rb, rb), None
 
@@ -69,7 +75,7 @@ def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, 
     if dtype == NVFP4:
         kq, kscale = quantize(k, g_k)
         vq, vscale = quantize(v, g_v)
-        krow, vrow = pack_nibbles(kq), pack_nibbles(vq)
+        krow = pack_nibbles(kq)
     else:
         krow = bf16_bits(k).view(np.uint8).reshape(k.shape[0], num_kv_heads, -1)
         vrow = bf16_bits(v).view(np.uint8).reshape(v.shape[0], num_kv_heads, -1)
@@ -80,11 +86,18 @@ def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, 
         for h in range(num_kv_heads):
             base = h * phb
             pool[page, base + k0 + slot * kb: base + k0 + (slot + 1) * kb] = krow[t, h]
-            pool[page, base + v0 + slot * vb: base + v0 + (slot + 1) * vb] = vrow[t, h]
             if dtype == NVFP4:
+                # this slot's nibble of every byte of its pair's row
+                row = pool[page, base + v0 + (slot // 2) * vb: base + v0 + (slot // 2 + 1) * vb]
+                if slot % 2 == 0:
+                    row[:] = (row & 0xF0) | vq[t, h]
+                else:
+                    row[:] = (row & 0x0F) | (vq[t, h] << 4)
                 (ko, ksb), (vo, vsb) = ks, vs
                 pool[page, base + ko + slot * ksb: base + ko + (slot + 1) * ksb] = kscale[t, h]
                 pool[page, base + vo + slot * vsb: base + vo + (slot + 1) * vsb] = vscale[t, h]
+            else:
+                pool[page, base + v0 + slot * vb: base + v0 + (slot + 1) * vb] = vrow[t, h]
     return pool
 
 
@@ -101,7 +114,7 @@ def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, sta
     if dtype == NVFP4:
         kq, kscale = quantize(k, g_k)
         vq, vscale = quantize(v, g_v)
-        krow, vrow = pack_nibbles(kq), pack_nibbles(vq)
+        krow = pack_nibbles(kq)
     else:
         krow = bf16_bits(k).view(np.uint8).reshape(T, num_kv_heads, -1)
         vrow = bf16_bits(v).view(np.uint8).reshape(T, num_kv_heads, -1)
@@ -109,12 +122,25 @@ def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, sta
         base = h * phb
         for j in range(kb):
             pool[pages, base + k0 + slots * kb + j] = krow[:, h, j]
-            pool[pages, base + v0 + slots * vb + j] = vrow[:, h, j]
         if dtype == NVFP4:
+            # even slots, then odd slots (the two halves of a pair share bytes)
+            for parity in (0, 1):
+                sel = (slots % 2) == parity
+                pg, sl = pages[sel], slots[sel]
+                for j in range(vb):
+                    col = base + v0 + (sl // 2) * vb + j
+                    old = pool[pg, col]
+                    if parity == 0:
+                        pool[pg, col] = (old & 0xF0) | vq[sel, h, j]
+                    else:
+                        pool[pg, col] = (old & 0x0F) | (vq[sel, h, j] << 4)
             (ko, ksb), (vo, vsb) = ks, vs
             for j in range(ksb):
                 pool[pages, base + ko + slots * ksb + j] = kscale[:, h, j]
                 pool[pages, base + vo + slots * vsb + j] = vscale[:, h, j]
+        else:
+            for j in range(vb):
+                pool[pages, base + v0 + slots * vb + j] = vrow[:, h, j]
     return pool
 
 
@@ -130,16 +156,19 @@ def gather_sequence(pool, dtype, num_kv_heads, head_dim, pages_of_seq, seq_len, 
     slots = t % PAGE
     base = head * phb
     kcols = base + k0 + slots[:, None] * kb + np.arange(kb)[None, :]
-    vcols = base + v0 + slots[:, None] * vb + np.arange(vb)[None, :]
     krow = pool[pages[:, None], kcols]
-    vrow = pool[pages[:, None], vcols]
     if dtype == NVFP4:
         (ko, ksb), (vo, vsb) = ks, vs
         kscol = base + ko + slots[:, None] * ksb + np.arange(ksb)[None, :]
         vscol = base + vo + slots[:, None] * vsb + np.arange(vsb)[None, :]
+        vcols = base + v0 + (slots[:, None] // 2) * vb + np.arange(vb)[None, :]
+        vbytes = pool[pages[:, None], vcols]
+        vcodes = np.where((slots % 2 == 0)[:, None], vbytes & 0xF, vbytes >> 4)
         kk = dequantize(unpack_nibbles(krow), pool[pages[:, None], kscol], g_k)
-        vv = dequantize(unpack_nibbles(vrow), pool[pages[:, None], vscol], g_v)
+        vv = dequantize(vcodes, pool[pages[:, None], vscol], g_v)
         return kk, vv
+    vcols = base + v0 + slots[:, None] * vb + np.arange(vb)[None, :]
+    vrow = pool[pages[:, None], vcols]
     kk = bf16_from_bits(krow.view(np.uint16))
     vv = bf16_from_bits(vrow.view(np.uint16))
     return kk, vv

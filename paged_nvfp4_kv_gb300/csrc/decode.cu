@@ -459,46 +459,50 @@ __device__ __forceinline__ void softmax_page(WarpState<NTW>& st, float (&s)[NTW]
   }
 }
 
-// O^T += V^T P^T for one page: NVFP4.
+// O^T += V^T P^T for one page: NVFP4.  V codes are stored slot-pair
+// interleaved (byte d of pair i holds element d of slots 2i and 2i+1), so one
+// byte widens to the (token 2i, token 2i+1) pair an A-fragment register holds.
+// Thread (gid, tig) covers dims 16*gid + mt (rows gid of m-tile mt, block gid)
+// and 128 + 16*gid + mt (rows gid+8, block 8+gid), tokens 2tig, 2tig+1 (pair
+// tig) and 2tig+8, 2tig+9 (pair tig+4).
 template <int NTW>
 __device__ __forceinline__ void pv_nvfp4(uint32_t sb, int lane, WarpState<NTW>& st,
                                          const uint32_t (&pb)[NTW][2], int page_lim) {
   const int gid = lane >> 2, tig = lane & 3;
-  const int t0 = 2 * tig, t1 = 2 * tig + 1, t2 = 2 * tig + 8, t3 = 2 * tig + 9;
-  // scales of blocks 2*gid, 2*gid+1 for the four tokens (zero when masked)
-  auto vscale = [&](int t) -> uint32_t {
-    const uint32_t two = lds16(sb + swz128(34 + (t >> 3), (t & 7) * 16 + 2 * gid));
-    return t < page_lim ? e4m3x2_to_f16x2(two) : 0u;
+  // scale pairs (token 2p, token 2p+1) of a block; masked tokens scale to 0
+  auto sbyte = [&](int t, int blk) -> uint32_t {
+    return t < page_lim ? lds8(sb + swz128(34 + (t >> 3), (t & 7) * 16 + blk)) : 0u;
   };
-  const uint32_t s0 = vscale(t0), s1 = vscale(t1), s2 = vscale(t2), s3 = vscale(t3);
-  const uint4 v0 = lds128(sb + swz128(18 + t0, 16 * gid));
-  const uint4 v1 = lds128(sb + swz128(18 + t1, 16 * gid));
-  const uint4 v2 = lds128(sb + swz128(18 + t2, 16 * gid));
-  const uint4 v3 = lds128(sb + swz128(18 + t3, 16 * gid));
-  const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
-  const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
-  uint32_t c0[4], c1[4], c2[4], c3[4];
+  const int t0 = 2 * tig, t2 = 2 * tig + 8;
+  const uint32_t s_a_lo = e4m3x2_to_f16x2(sbyte(t0, gid) | (sbyte(t0 + 1, gid) << 8));
+  const uint32_t s_a_hi = e4m3x2_to_f16x2(sbyte(t0, 8 + gid) | (sbyte(t0 + 1, 8 + gid) << 8));
+  const uint32_t s_b_lo = e4m3x2_to_f16x2(sbyte(t2, gid) | (sbyte(t2 + 1, gid) << 8));
+  const uint32_t s_b_hi = e4m3x2_to_f16x2(sbyte(t2, 8 + gid) | (sbyte(t2 + 1, 8 + gid) << 8));
+  // pair row p = box rows 18 + 2p (dims 0..127) and 19 + 2p (dims 128..255)
+  const uint4 a_lo = lds128(sb + swz128(18 + 2 * tig, 16 * gid));
+  const uint4 a_hi = lds128(sb + swz128(19 + 2 * tig, 16 * gid));
+  const uint4 b_lo = lds128(sb + swz128(26 + 2 * tig, 16 * gid));
+  const uint4 b_hi = lds128(sb + swz128(27 + 2 * tig, 16 * gid));
+  const uint32_t wal[4] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w}, wah[4] = {a_hi.x, a_hi.y, a_hi.z, a_hi.w};
+  const uint32_t wbl[4] = {b_lo.x, b_lo.y, b_lo.z, b_lo.w}, wbh[4] = {b_hi.x, b_hi.y, b_hi.z, b_hi.w};
 #pragma unroll
-  for (int mt = 0; mt < 16; ++mt) {
-    const uint32_t sel = (mt < 8) ? 0x1010u : 0x3232u;  // block 2*gid or 2*gid+1
-    const int wi = mt >> 2, bi = mt & 3;
-    if (bi == 0) {
-      e2m1x8_unpack(w0[wi], c0);
-      e2m1x8_unpack(w1[wi], c1);
-      e2m1x8_unpack(w2[wi], c2);
-      e2m1x8_unpack(w3[wi], c3);
+  for (int wi = 0; wi < 4; ++wi) {
+    uint32_t c0[4], c1[4], c2[4], c3[4];
+    e2m1x8_unpack(wal[wi], c0);
+    e2m1x8_unpack(wah[wi], c1);
+    e2m1x8_unpack(wbl[wi], c2);
+    e2m1x8_unpack(wbh[wi], c3);
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      const int mt = 4 * wi + bi;  // byte mt of each chunk
+      uint32_t af[4];
+      af[0] = hmul2(c0[bi], s_a_lo);  // dim 16*gid + mt,       tokens 2tig, 2tig+1
+      af[1] = hmul2(c1[bi], s_a_hi);  // dim 128 + 16*gid + mt
+      af[2] = hmul2(c2[bi], s_b_lo);  // tokens 2tig+8, 2tig+9
+      af[3] = hmul2(c3[bi], s_b_hi);
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pb[nt][0], pb[nt][1]);
     }
-    const uint32_t x = hmul2(c0[bi], prmt(s0, s0, sel));
-    const uint32_t y = hmul2(c1[bi], prmt(s1, s1, sel));
-    const uint32_t z = hmul2(c2[bi], prmt(s2, s2, sel));
-    const uint32_t w = hmul2(c3[bi], prmt(s3, s3, sel));
-    uint32_t af[4];
-    af[0] = prmt(x, y, 0x5410u);  // dim 32*gid + 2*mt,     tokens 2tig, 2tig+1
-    af[1] = prmt(x, y, 0x7632u);  // dim 32*gid + 2*mt + 1
-    af[2] = prmt(z, w, 0x5410u);  // tokens 2tig+8, 2tig+9
-    af[3] = prmt(z, w, 0x7632u);
-#pragma unroll
-    for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pb[nt][0], pb[nt][1]);
   }
 }
 
@@ -734,10 +738,24 @@ __global__ void __launch_bounds__(NW * 32, 1)
           for (int c = 0; c < 2; ++c) {
             const int row = row_base + 8 * nt + 2 * tig + c;
 #pragma unroll
-            for (int mt = 0; mt < 16; ++mt) {
-              const int d = 32 * gid + 2 * mt;
+            // pairs of adjacent dims: bf16 m-tile mt holds dims 32*gid + 2*mt
+            // (c) and +1 (c + 2); NVFP4 m-tiles mt, mt+1 hold dims 16*gid + mt,
+            // +1 (c) and 128 + 16*gid + mt, +1 (c + 2)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              int d;
+              float2 v;
+              const float w = wgt[nt][c];
+              if (KVDT == PNKV_KV_NVFP4) {
+                const int mt = j & ~1;
+                const int e = (j & 1) ? c + 2 : c;
+                d = ((j & 1) ? 128 : 0) + 16 * gid + mt;
+                v = make_float2(st.o[mt][nt][e] * w, st.o[mt + 1][nt][e] * w);
+              } else {
+                d = 32 * gid + 2 * j;
+                v = make_float2(st.o[j][nt][c] * w, st.o[j][nt][c + 2] * w);
+              }
               float2* dst = reinterpret_cast<float2*>(mbuf + merge_pos(row, d));
-              const float2 v = make_float2(st.o[mt][nt][c] * wgt[nt][c], st.o[mt][nt][c + 2] * wgt[nt][c]);
               if (k == 0) {
                 *dst = v;
               } else {

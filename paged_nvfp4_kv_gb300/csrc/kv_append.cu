@@ -188,7 +188,16 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
       const uint32_t kc = quantize8(kx, a.k_scale, &ks);
       const uint32_t vc = quantize8(vx, a.v_scale, &vs);
       reinterpret_cast<uint32_t*>(rec + slot * 128)[lane] = kc;
-      reinterpret_cast<uint32_t*>(rec + 2304 + slot * 128)[lane] = vc;
+      // V codes: this slot's nibble of bytes 8*lane .. 8*lane+7 of its pair
+      // row; the pair's other slot may be written concurrently, so the two
+      // nibble sets are replaced with atomics that leave the other untouched
+      uint64_t bits = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) bits |= static_cast<uint64_t>((vc >> (4 * e)) & 0xFu) << (8 * e);
+      const int sh = 4 * (slot & 1);
+      unsigned long long* vw = reinterpret_cast<unsigned long long*>(rec + 2304 + (slot >> 1) * 256) + lane;
+      atomicAnd(vw, ~(0x0F0F0F0F0F0F0F0Full << sh));
+      atomicOr(vw, static_cast<unsigned long long>(bits << sh));
       if ((lane & 1) == 0) {
         rec[2048 + slot * 16 + (lane >> 1)] = static_cast<uint8_t>(ks);
         rec[4352 + slot * 16 + (lane >> 1)] = static_cast<uint8_t>(vs);

@@ -104,8 +104,9 @@ def test_chunked_equals_dense(monkeypatch):
 def test_page_layout_offsets_by_hand():
     """Token 37 of a sequence whose page table is [5, 2, 9] lives in page 9,
     slot 5.  For KV head 1 of an NVFP4 page (4,608 bytes per head record):
-    K codes at 4608 + 5*128, K scales at 4608 + 2048 + 5*16, V codes at
-    4608 + 2304 + 5*128, V scales at 4608 + 4352 + 5*16."""
+    K codes at 4608 + 5*128, K scales at 4608 + 2048 + 5*16, V codes in the
+    high nibbles (odd slot) of slot pair 2 at 4608 + 2304 + 2*256, V scales at
+    4608 + 4352 + 5*16."""
     pool = PG.new_pool(12, PG.NVFP4, 4, D)
     assert pool.shape == (12, 18432)
     k = np.zeros((1, 4, D))
@@ -119,13 +120,20 @@ def test_page_layout_offsets_by_hand():
     off = nz % 18432
     kc = range(4608 + 640, 4608 + 768)
     ks = range(4608 + 2048 + 80, 4608 + 2048 + 96)
-    vc = range(4608 + 2304 + 640, 4608 + 2304 + 768)
+    vc = range(4608 + 2304 + 512, 4608 + 2304 + 768)
     vs = range(4608 + 4352 + 80, 4608 + 4352 + 96)
     assert set(off) == set(kc) | set(ks) | set(vc) | set(vs)
     # 1.0 with g = 1: scale = e4m3(1/6) (code 0x23 = 2**-3 * 1.375 = 0.171875),
-    # element 1/0.171875 = 5.82 -> code 7 (6.0); both nibbles -> 0x77; V -> 0xFF
-    assert pool[9, 4608 + 640] == 0x77 and pool[9, 4608 + 2304 + 640] == 0xFF
+    # element 1/0.171875 = 5.82 -> code 7 (6.0); both nibbles -> 0x77; V -1.0
+    # -> code 15 in the high nibble of every byte of the pair row -> 0xF0
+    assert pool[9, 4608 + 640] == 0x77
+    assert np.all(pool[9, 4608 + 2304 + 512: 4608 + 2304 + 768] == 0xF0)
     assert pool[9, 4608 + 2048 + 80] == 0x23 and pool[9, 4608 + 4352 + 80] == 0x23
+    # the even slot of the same pair fills the low nibbles without touching
+    # the odd slot's
+    v[0, 1, :] = 1.0
+    PG.scatter_tokens(pool, PG.NVFP4, 4, D, np.array([[5, 2, 9]]), [0], [36], k, v, 1.0, 1.0)
+    assert np.all(pool[9, 4608 + 2304 + 512: 4608 + 2304 + 768] == 0xF7)
 
 
 def test_bf16_page_layout_offsets_by_hand():

@@ -37,8 +37,8 @@ ALGO_BYTES_PER_TOKEN = {"nvfp4": 4 * 2 * (128 + 16), "bf16": 4 * 2 * 256 * 2}
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", type=int, default=3, help="workload number (1..4)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -77,7 +77,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -114,6 +114,28 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def profiled_traffic(kv_dtype):
+    """DRAM bytes per decode launch from the committed ncu summary, or None when
+    the decode kernel's source changed since that capture."""
+    import hashlib
+    if kv_dtype != "nvfp4":
+        return None
+    path = os.path.join(ROOT, "profiles", "paged_decode_nvfp4_1M_keys.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        line = line.strip()
+        for key in ("traffic_bytes_per_launch:", "source_sha256_16:"):
+            if line.startswith(key):
+                vals[key] = line.split(":", 1)[1].strip()
+    src = b"".join(open(os.path.join(ROOT, "paged_nvfp4_kv_gb300", "csrc", f), "rb").read()
+                   for f in ("decode.cu", "device_common.cuh"))
+    if hashlib.sha256(src).hexdigest()[:16] != vals.get("source_sha256_16:"):
+        return None
+    return int(vals["traffic_bytes_per_launch:"])
 
 
 def workload(cfg):
@@ -221,9 +243,7 @@ def run_ours(args):
         s.fill()
     torch.cuda.synchronize()
 
-    # events around each call of the step, on the launching stream
     K, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     with torch.cuda.stream(stream):
         for _ in range(W):
             s.step()
@@ -231,27 +251,34 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # the headline: K whole steps back to back, events only around the loop
     clocks = ClockSampler(local)
     with clocks:
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             start.record(stream)
-            for i in range(K):
-                ev[i][0].record(stream)
-                s.append()
-                ev[i][1].record(stream)
-                w_ = s.w
-                paged_decode_attention(s.cache, s.q_roped, s.qo_indptr, s.page_table, s.seq_lens,
-                                       w_.num_q_heads, s.max_qlen, s.sm_scale, w_.causal, s.o_part,
-                                       s.lse_part, s.work_meta, s.dev_err, stream)
-                ev[i][2].record(stream)
-                split_kv_combine(s.o_part, s.lse_part, s.work_meta, s.qo_indptr, s.total_q,
-                                 w_.num_q_heads, w_.num_kv_heads, s.max_qlen, s.out, s.lse, stream)
-                ev[i][3].record(stream)
+            for _ in range(K):
+                s.step()
             stop.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
+    # per-kernel times: a second pass with events between the three calls
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            ev[i][0].record(stream)
+            s.append()
+            ev[i][1].record(stream)
+            w_ = s.w
+            paged_decode_attention(s.cache, s.q_roped, s.qo_indptr, s.page_table, s.seq_lens,
+                                   w_.num_q_heads, s.max_qlen, s.sm_scale, w_.causal, s.o_part,
+                                   s.lse_part, s.work_meta, s.dev_err, stream)
+            ev[i][2].record(stream)
+            split_kv_combine(s.o_part, s.lse_part, s.work_meta, s.qo_indptr, s.total_q,
+                             w_.num_q_heads, w_.num_kv_heads, s.max_qlen, s.out, s.lse, stream)
+            ev[i][3].record(stream)
+    stream.synchronize()
     total_ms = start.elapsed_time(stop)
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -314,7 +341,8 @@ def run_ours(args):
                        "split_kv_combine": combine_ms},
         "hbm_gbs_decode": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.kv_dtype),
+                     "peak_kind": peak_kind,
                      "kernel": "paged_decode_attention",
                      "algorithmic_bytes_per_launch": algo_bytes},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

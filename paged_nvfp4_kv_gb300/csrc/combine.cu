@@ -8,7 +8,6 @@
 // A split with lse_s = -inf (no visible key) weighs 0; a row with no visible
 // key at all gets out = 0 and lse = -inf.
 //
-// One warp per (query token, query head) row; lane l owns dims 8l .. 8l+7.
 // The partials are read once, coalesced (1 KiB per split per row).
 #include <cmath>
 
@@ -31,11 +30,20 @@ struct CombineArgs {
   float* lse_out;
 };
 
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = a.total_q * a.hq;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (row >= rows) return;
+// One 64-thread block per output row; thread j owns dims 4j .. 4j+3.  The
+// split weights are formed once in shared memory, then every thread streams
+// its float4 of each split (independent loads, so many are in flight).
+constexpr int kThreads = 64;
+constexpr int kMaxCached = 1024;  // splits whose weights fit in shared memory
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
+  __shared__ float w_s[kMaxCached];
+  __shared__ float red[kThreads / 32];
+  __shared__ float bcast[2];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
   const int64_t t = row / a.hq;
   const int h = static_cast<int>(row - t * a.hq);
   // sequence of token t: last b with qo_indptr[b] <= t
@@ -48,46 +56,73 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   const int b = lo;
   const int64_t seg = static_cast<int64_t>(b) * a.hkv + h / a.group;
   const int32_t first = __ldg(a.meta + 4 + 2 * seg);
-  const int32_t cnt = __ldg(a.meta + 4 + 2 * seg + 1);
+  int32_t cnt = __ldg(a.meta + 4 + 2 * seg + 1);
   const int r = static_cast<int>((t - __ldg(a.qo_indptr + b)) * a.group + h % a.group);
-  const bool ok = cnt > 0 && first >= 0 && r < a.rows_per_slot;
+  if (!(cnt > 0 && first >= 0 && r < a.rows_per_slot)) cnt = 0;
+  const float* lse = a.lse_part + static_cast<int64_t>(first) * a.rows_per_slot + r;
 
+  // M = max_s lse_s
   float M = -INFINITY;
-  if (ok)
-    for (int s = lane; s < cnt; s += 32) M = fmaxf(M, __ldg(a.lse_part + static_cast<int64_t>(first + s) * a.rows_per_slot + r));
+  for (int s = tid; s < cnt; s += kThreads) M = fmaxf(M, __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = fmaxf(red[0], red[1]);
+  __syncthreads();
+  // weights e^(lse_s - M) and their sum
   float wsum = 0.f;
-  if (ok && M != -INFINITY) {
-    for (int s = 0; s < cnt; ++s) {
-      const int64_t pr = static_cast<int64_t>(first + s) * a.rows_per_slot + r;
-      const float l = __ldg(a.lse_part + pr);
-      if (l == -INFINITY) continue;
-      const float w = expf(l - M);
+  if (M != -INFINITY) {
+    for (int s = tid; s < cnt; s += kThreads) {
+      const float l = __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot);
+      const float w = (l == -INFINITY) ? 0.f : expf(l - M);
+      if (s < kMaxCached) w_s[s] = w;
       wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(a.o_part + pr * 256) + 2 * lane;
-      const float4 x = __ldg(src), y = __ldg(src + 1);
-      acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-      acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] *= inv;
-  const int64_t base = row * 256 + 8 * lane;
-  if (a.out_fp32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + base);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  } else {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) w[e] = f32_to_bf16_bits(acc[2 * e]) | (f32_to_bf16_bits(acc[2 * e + 1]) << 16);
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + base) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane == 0) red[warp] = wsum;
+  __syncthreads();
+  if (tid == 0) bcast[0] = red[0] + red[1];
+  __syncthreads();
+  wsum = bcast[0];
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (wsum > 0.f) {
+    const float4* src = reinterpret_cast<const float4*>(
+        a.o_part + (static_cast<int64_t>(first) * a.rows_per_slot + r) * 256) + tid;
+    const int64_t step = static_cast<int64_t>(a.rows_per_slot) * 64;  // float4s per slot
+#pragma unroll 4
+    for (int s = 0; s < cnt; ++s) {
+      float w;
+      if (s < kMaxCached) {
+        w = w_s[s];
+      } else {
+        const float l = __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot);
+        w = (l == -INFINITY) ? 0.f : expf(l - M);
+      }
+      const float4 x = __ldg(src + s * step);
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+    }
+    const float inv = 1.f / wsum;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
   }
-  if (a.lse_out && lane == 0) a.lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  const int64_t base = row * 256 + 4 * tid;
+  if (a.out_fp32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + base) = acc;
+  } else {
+    const uint32_t w0 = f32_to_bf16_bits(acc.x) | (f32_to_bf16_bits(acc.y) << 16);
+    const uint32_t w1 = f32_to_bf16_bits(acc.z) | (f32_to_bf16_bits(acc.w) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + base) = make_uint2(w0, w1);
+  }
+  if (a.lse_out && tid == 0) a.lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
 }  // namespace
@@ -120,8 +155,7 @@ extern "C" int split_kv_combine(const float* o_part, const float* lse_part, cons
   a.out_fp32 = out_is_fp32 ? 1 : 0;
   a.lse_out = lse_out;
   const int64_t rows = total_q * num_q_heads;
-  const int64_t blocks = (rows + 7) / 8;
-  if (blocks > 2147483647LL) return PNKV_ERR_INVALID_ARG;
-  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(a);
-  return launch_status();
+  if (rows > 2147483647LL) return PNKV_ERR_INVALID_ARG;
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0,
+                    as_stream(stream), a);
 }

@@ -570,6 +570,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
   if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap);
   __syncthreads();
+  griddep_wait();  // the previous kernel's writes (pool, queries) are visible from here
+  griddep_launch_dependents();
 
   // this CTA's unit range
   const int64_t total = total_units(a, lane);
@@ -848,8 +850,7 @@ int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
       return PNKV_ERR_CUDA;
     configured = true;
   }
-  kern<<<grid, NW * 32, P::kDynamicBytes, stream>>>(map, a);
-  return launch_status();
+  return launch_pdl(kern, dim3(grid), dim3(NW * 32), P::kDynamicBytes, stream, map, a);
 }
 
 template <int KVDT>

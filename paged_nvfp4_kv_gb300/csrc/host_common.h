@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "pnkv.h"
@@ -19,6 +20,26 @@ inline bool aligned(const void* p, uintptr_t a) {
 // Status of the most recent launch on this thread.
 inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? PNKV_OK : PNKV_ERR_CUDA;
+}
+
+// Launch `kernel` with programmatic stream serialisation, so that its
+// launch and prologue overlap the tail of the previous kernel in the stream
+// (the kernel waits with griddepcontrol.wait before touching global memory).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? PNKV_OK
+                                                                                       : PNKV_ERR_CUDA;
 }
 
 // SM count of the current device (cached per device id).

@@ -133,6 +133,8 @@ __device__ __forceinline__ void rope8(float (&x)[8], const uint4& raw, int lane,
 }
 
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps_per_block = blockDim.x >> 5;
   const int hq = a.q ? a.num_q_heads : 0;
@@ -267,6 +269,6 @@ extern "C" int kv_append_nvfp4(const pnkv_cache* cache, const int32_t* page_tabl
   int64_t blocks = (rows + 7) / 8;
   const int64_t cap = static_cast<int64_t>(sms) * 16;
   if (blocks > cap) blocks = cap;
-  kv_append_kernel<<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(a);
-  return launch_status();
+  return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                    as_stream(stream), a);
 }

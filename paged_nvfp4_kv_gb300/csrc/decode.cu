@@ -228,16 +228,20 @@ struct Walker {
 // then waits on a stage whose previous round it consumed itself, i.e. never
 // more than one barrier phase ahead (a parity wait cannot tell phase k from
 // phase k + 2, so a wait two phases ahead would pass on stale data).
-template <int KVDT, int NTW, int RG, int NW>
+template <int KVDT, int NTW, int RG, int NW, int QS>
 struct Plan {
   static constexpr int kStreams = Consumers<NW, RG>::kWarps / RG;   // warps that split the units
   static constexpr int kRows = 8 * NTW * RG;             // query rows per KV head handled
   static constexpr int kMergeBytes = kRows * 256 * 4;
   static constexpr int kMlBytes = kStreams * kRows * 2 * 4;
-  static constexpr int kFixed = kMergeBytes + kMlBytes + 1024 /*align*/ + 1024 /*bars, flags*/;
+  static constexpr int kQBytes = QS ? NTW * RG * 16 * 32 * 8 : 0;  // Q fragments in shared memory
+  static constexpr int kFixed = kMergeBytes + kMlBytes + kQBytes + 1024 /*align*/ + 1024 /*bars, flags*/;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kStagesFit = (kMaxSmem - kFixed) / Geometry<KVDT>::kStageBytes;
-  static constexpr int kStagesCap = kStagesFit < 48 ? kStagesFit : 48;
+#ifndef PNKV_MAX_STAGES
+#define PNKV_MAX_STAGES 48
+#endif
+  static constexpr int kStagesCap = kStagesFit < PNKV_MAX_STAGES ? kStagesFit : PNKV_MAX_STAGES;
   static constexpr int kStages = (kStagesCap / kStreams) * kStreams;
   static constexpr int kStageRegion = kStages * Geometry<KVDT>::kStageBytes;
   static constexpr int kBarOff = kStageRegion;                 // full[S], empty[S]
@@ -245,7 +249,8 @@ struct Plan {
   static constexpr int kAbortOff = kMetaOff + 4 * kStages;     // int32 abort flag
   static constexpr int kMlOff = (kAbortOff + 4 + 15) & ~15;
   static constexpr int kMergeOff = (kMlOff + kMlBytes + 15) & ~15;
-  static constexpr int kTotal = kMergeOff + kMergeBytes;
+  static constexpr int kQOff = kMergeOff + kMergeBytes;
+  static constexpr int kTotal = kQOff + kQBytes;
   static constexpr int kDynamicBytes = kTotal + 1024;          // room to align the base
   static_assert(kStages >= 2 * kStreams, "every consumer stream needs two stages");
   static_assert(kStages % kStreams == 0, "stages must split evenly over the streams");
@@ -282,6 +287,26 @@ struct WarpState {
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
     }
+  }
+};
+
+// Query B-fragments, held in registers (QS = 0) or in shared memory (QS = 1,
+// fragment order [n-tile][k-step][lane] x 8 bytes, read with one 64-bit load
+// per k-step; frees 32 registers per n-tile for more resident warps).
+template <int NTW, int QS>
+struct QFrag;
+template <int NTW>
+struct QFrag<NTW, 0> {
+  uint32_t r[NTW][16][2];
+  __device__ __forceinline__ uint2 get(int nt, int kk) const { return make_uint2(r[nt][kk][0], r[nt][kk][1]); }
+};
+template <int NTW>
+struct QFrag<NTW, 1> {
+  uint32_t base;  // shared address of this warp's first n-tile, lane offset included
+  __device__ __forceinline__ uint2 get(int nt, int kk) const {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(base + (nt * 16 + kk) * 256));
+    return v;
   }
 };
 
@@ -322,13 +347,28 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, const Piece& pc, int
   }
 }
 
+template <int NTW>
+__device__ __forceinline__ void set_qfrag_base(QFrag<NTW, 1>& q, uint32_t base) { q.base = base; }
+template <int NTW>
+__device__ __forceinline__ void set_qfrag_base(QFrag<NTW, 0>&, uint32_t) {}
+template <int KVDT, int NTW>
+__device__ __forceinline__ void load_q_regs(const DecodeArgs& a, const Piece& pc, int row_base, int lane,
+                                            QFrag<NTW, 0>& q) {
+  load_q<KVDT, NTW>(a, pc, row_base, lane, q.r);
+}
+template <int KVDT, int NTW>
+__device__ __forceinline__ void load_q_regs(const DecodeArgs&, const Piece&, int, int, QFrag<NTW, 1>&) {}
+
 // S^T (16 tokens x 8 rows per n-tile) for one page: NVFP4.  The 16 k-steps
 // feed four independent accumulator sets (k-step mod 4) so that consecutive
 // MMAs do not wait on each other; the sets are summed at the end.
-template <int NTW>
-__device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const uint32_t (&qb)[NTW][16][2],
-                                         float (&s)[NTW][4]) {
+#ifndef PNKV_QK_ACC
+#define PNKV_QK_ACC 2
+#endif
+template <int NTW, typename Q>
+__device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const Q& qf, float (&s)[NTW][4]) {
   const int gid = lane >> 2, tig = lane & 3;
+  constexpr int NA = PNKV_QK_ACC;  // independent accumulator sets (k-step mod NA)
   float acc[4][NTW][4];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
@@ -364,7 +404,10 @@ __device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const uint32_t (
         af[2] = hmul2(cl[2 * half + 1], scl);
         af[3] = hmul2(ch[2 * half + 1], sch);
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(acc[kk & 3][nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+        for (int nt = 0; nt < NTW; ++nt) {
+          const uint2 qv = qf.get(nt, kk);
+          mma_f16_16816(acc[kk % NA][nt], af, qv.x, qv.y);
+        }
       }
     }
   }
@@ -375,9 +418,8 @@ __device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const uint32_t (
 }
 
 // S^T for one page: bf16 cache (four independent accumulator sets, as above).
-template <int NTW>
-__device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const uint32_t (&qb)[NTW][16][2],
-                                        float (&s)[NTW][4]) {
+template <int NTW, typename Q>
+__device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const Q& qf, float (&s)[NTW][4]) {
   const int gid = lane >> 2, tig = lane & 3;
   float acc[4][NTW][4];
 #pragma unroll
@@ -392,14 +434,18 @@ __device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const uint32_t (&
     {
       const uint32_t af[4] = {klo.x, khi.x, klo.y, khi.y};
 #pragma unroll
-      for (int nt = 0; nt < NTW; ++nt)
-        mma_bf16_16816(acc[(2 * c) & 3][nt], af, qb[nt][2 * c][0], qb[nt][2 * c][1]);
+      for (int nt = 0; nt < NTW; ++nt) {
+        const uint2 qv = qf.get(nt, 2 * c);
+        mma_bf16_16816(acc[(2 * c) & 3][nt], af, qv.x, qv.y);
+      }
     }
     {
       const uint32_t af[4] = {klo.z, khi.z, klo.w, khi.w};
 #pragma unroll
-      for (int nt = 0; nt < NTW; ++nt)
-        mma_bf16_16816(acc[(2 * c + 1) & 3][nt], af, qb[nt][2 * c + 1][0], qb[nt][2 * c + 1][1]);
+      for (int nt = 0; nt < NTW; ++nt) {
+        const uint2 qv = qf.get(nt, 2 * c + 1);
+        mma_bf16_16816(acc[(2 * c + 1) & 3][nt], af, qv.x, qv.y);
+      }
     }
   }
 #pragma unroll
@@ -408,25 +454,31 @@ __device__ __forceinline__ void qk_bf16(uint32_t sb, int lane, const uint32_t (&
     for (int e = 0; e < 4; ++e) s[nt][e] = (acc[0][nt][e] + acc[1][nt][e]) + (acc[2][nt][e] + acc[3][nt][e]);
 }
 
-// Online softmax on the page's logits; returns the P^T B-fragments.
-template <int NTW>
-__device__ __forceinline__ void softmax_page(WarpState<NTW>& st, float (&s)[NTW][4], float scale,
-                                             int32_t key0, int32_t page_lim, bool masked, int lane,
-                                             uint32_t (&pb)[NTW][2]) {
+// Online softmax over the logits of NP pages at once (one max reduction and
+// one accumulator rescale per call); returns the P^T B-fragments per page.
+template <int NTW, int NP>
+__device__ __forceinline__ void softmax_pages(WarpState<NTW>& st, float (&s)[NP][NTW][4], float scale,
+                                              const int32_t (&key0)[NP], const int32_t (&page_lim)[NP],
+                                              const bool (&masked)[NP], int lane,
+                                              uint32_t (&pb)[NP][NTW][2]) {
   const int gid = lane >> 2;
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt) {
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] *= scale;
-    if (masked) {
+    for (int pg = 0; pg < NP; ++pg) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = gid + ((e & 2) ? 8 : 0);
-        const int key = key0 + tok;
-        if (tok >= page_lim || key >= st.lim[nt][e & 1]) s[nt][e] = -INFINITY;
+      for (int e = 0; e < 4; ++e) s[pg][nt][e] *= scale;
+      if (masked[pg]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = gid + ((e & 2) ? 8 : 0);
+          if (tok >= page_lim[pg] || key0[pg] + tok >= st.lim[nt][e & 1]) s[pg][nt][e] = -INFINITY;
+        }
       }
+      mx0 = fmaxf(mx0, fmaxf(s[pg][nt][0], s[pg][nt][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[pg][nt][1], s[pg][nt][3]));
     }
-    float mx0 = fmaxf(s[nt][0], s[nt][2]), mx1 = fmaxf(s[nt][1], s[nt][3]);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -438,12 +490,20 @@ __device__ __forceinline__ void softmax_page(WarpState<NTW>& st, float (&s)[NTW]
     const float al0 = fast_exp2(st.m[nt][0] - base0), al1 = fast_exp2(st.m[nt][1] - base1);
     st.m[nt][0] = mn0;
     st.m[nt][1] = mn1;
-    const uint32_t x0 = f32x2_to_f16x2(fast_exp2(s[nt][0] - base0), fast_exp2(s[nt][1] - base1));
-    const uint32_t x1 = f32x2_to_f16x2(fast_exp2(s[nt][2] - base0), fast_exp2(s[nt][3] - base1));
-    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x0));
-    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x1));
-    st.l[nt][0] = st.l[nt][0] * al0 + (f0.x + f1.x);
-    st.l[nt][1] = st.l[nt][1] * al1 + (f0.y + f1.y);
+    float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const uint32_t x0 = f32x2_to_f16x2(fast_exp2(s[pg][nt][0] - base0), fast_exp2(s[pg][nt][1] - base1));
+      const uint32_t x1 = f32x2_to_f16x2(fast_exp2(s[pg][nt][2] - base0), fast_exp2(s[pg][nt][3] - base1));
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x0));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x1));
+      add0 += f0.x + f1.x;
+      add1 += f0.y + f1.y;
+      pb[pg][nt][0] = movmatrix_trans(x0);
+      pb[pg][nt][1] = movmatrix_trans(x1);
+    }
+    st.l[nt][0] = st.l[nt][0] * al0 + add0;
+    st.l[nt][1] = st.l[nt][1] * al1 + add1;
     // rescale the accumulators only when some column's running max moved
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
@@ -454,8 +514,6 @@ __device__ __forceinline__ void softmax_page(WarpState<NTW>& st, float (&s)[NTW]
         st.o[mt][nt][3] *= al1;
       }
     }
-    pb[nt][0] = movmatrix_trans(x0);
-    pb[nt][1] = movmatrix_trans(x1);
   }
 }
 
@@ -541,10 +599,10 @@ __device__ __forceinline__ void pv_bf16(uint32_t sb, int lane, WarpState<NTW>& s
 
 // ---------------------------------------------------------------------------
 
-template <int KVDT, int NTW, int RG, int NW>
+template <int KVDT, int NTW, int RG, int NW, int QS, int NP>
 __global__ void __launch_bounds__(NW * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
-  using P = Plan<KVDT, NTW, RG, NW>;
+  using P = Plan<KVDT, NTW, RG, NW, QS>;
   using C = Consumers<NW, RG>;
   constexpr int kProducerWarp = NW - 1;
   using Geo = Geometry<KVDT>;
@@ -660,11 +718,27 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int row_base = rg * 8 * NTW;
   const int gid = lane >> 2, tig = lane & 3;
   WarpState<NTW> st;
-  uint32_t qb[NTW][16][2];
+  QFrag<NTW, QS> qf;
 
   while (walk.next(a, &pc)) {
     const int rows = a.group * pc.s.qlen;
-    load_q<KVDT, NTW>(a, pc, row_base, lane, qb);
+    if (QS) {
+      // one warp per row group stages the fragments; the others wait for it
+      if (stream == 0) {
+        uint32_t tmp[NTW][16][2];
+        load_q<KVDT, NTW>(a, pc, row_base, lane, tmp);
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            *reinterpret_cast<uint2*>(smem + P::kQOff + (((rg * NTW + nt) * 16 + kk) * 32 + lane) * 8) =
+                make_uint2(tmp[nt][kk][0], tmp[nt][kk][1]);
+      }
+      named_bar_sync(1, C::kThreads);
+      set_qfrag_base(qf, smem_addr(smem + P::kQOff + (rg * NTW * 16 * 32 + lane) * 8));
+    } else {
+      load_q_regs<KVDT, NTW>(a, pc, row_base, lane, qf);
+    }
     st.reset();
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
@@ -674,32 +748,59 @@ __global__ void __launch_bounds__(NW * 32, 1)
         st.lim[nt][c] = a.causal ? pc.s.len - pc.s.qlen + n / a.group + 1 : pc.s.len;
       }
     const int32_t mask_from = a.causal ? pc.s.len - pc.s.qlen + 1 : pc.s.len;  // first key some row cannot see
-    // units of this piece owned by this warp
-    int64_t i = pc.i0 + ((stream - pc.i0 % P::kStreams) % P::kStreams + P::kStreams) % P::kStreams;
-    for (; i < pc.i0 + pc.n; i += P::kStreams) {
-      const int s = static_cast<int>(i % P::kStages);
-      const uint32_t par = static_cast<uint32_t>((i / P::kStages) & 1);
-      if (*abort_flag || !mbar_wait(&full[s], par)) {
+    // units of this piece owned by this warp, NP per iteration: i, i + S, ...
+    // (missing trailing units are stand-ins for unit i, fully masked)
+    constexpr int64_t S = P::kStreams;
+    const int64_t end = pc.i0 + pc.n;
+    int64_t i = pc.i0 + ((stream - pc.i0 % S) % S + S) % S;
+    for (; i < end; i += NP * S) {
+      int64_t u[NP];
+      bool here[NP];
+      int st_idx[NP];
+      bool okw = !*abort_flag;
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        here[pg] = i + pg * S < end;
+        u[pg] = here[pg] ? i + pg * S : i;
+        st_idx[pg] = static_cast<int>(u[pg] % P::kStages);
+        if (okw && here[pg])
+          okw = mbar_wait(&full[st_idx[pg]], static_cast<uint32_t>((u[pg] / P::kStages) & 1));
+      }
+      if (!okw) {
         if (lane == 0) flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
       }
-      if (stage_valid[s]) {
-        const int32_t page_idx = pc.p0 + static_cast<int32_t>(i - pc.i0);
-        const int32_t key0 = page_idx * 16;
-        const int32_t page_lim = pc.s.len - key0;           // valid tokens in the page
-        const bool masked = key0 + 16 > mask_from;
-        const uint32_t sb = smem_addr(smem + s * Geo::kStageBytes);
-        float sacc[NTW][4];
-        uint32_t pb[NTW][2];
-        if (KVDT == PNKV_KV_NVFP4) qk_nvfp4<NTW>(sb, lane, qb, sacc);
-        else qk_bf16<NTW>(sb, lane, qb, sacc);
-        softmax_page<NTW>(st, sacc, a.qk_scale_log2, key0, page_lim, masked, lane, pb);
-        if (KVDT == PNKV_KV_NVFP4) pv_nvfp4<NTW>(sb, lane, st, pb, page_lim);
-        else pv_bf16<NTW>(sb, lane, st, pb, page_lim);
+      int32_t key0[NP], page_lim[NP];
+      bool masked[NP];
+      uint32_t sb[NP];
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        const int32_t page_idx = pc.p0 + static_cast<int32_t>(u[pg] - pc.i0);
+        key0[pg] = page_idx * 16;
+        const bool live = here[pg] && stage_valid[st_idx[pg]];
+        page_lim[pg] = live ? pc.s.len - key0[pg] : 0;  // valid tokens in the page
+        masked[pg] = !live || key0[pg] + 16 > mask_from;
+        sb[pg] = smem_addr(smem + st_idx[pg] * Geo::kStageBytes);
+      }
+      float sacc[NP][NTW][4];
+      uint32_t pb[NP][NTW][2];
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        if (KVDT == PNKV_KV_NVFP4) qk_nvfp4<NTW>(sb[pg], lane, qf, sacc[pg]);
+        else qk_bf16<NTW>(sb[pg], lane, qf, sacc[pg]);
+      }
+      softmax_pages<NTW, NP>(st, sacc, a.qk_scale_log2, key0, page_lim, masked, lane, pb);
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        if (KVDT == PNKV_KV_NVFP4) pv_nvfp4<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
+        else pv_bf16<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0)
+#pragma unroll
+        for (int pg = 0; pg < NP; ++pg)
+          if (here[pg]) mbar_arrive(&empty[st_idx[pg]]);
     }
 
     // ---- merge the warps' partial states (fixed order) and write the slot
@@ -839,10 +940,13 @@ int make_pool_map(const pnkv_cache* c, int box_rows, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? PNKV_OK : PNKV_ERR_CUDA;
 }
 
-template <int KVDT, int NTW, int RG, int NW>
+// NP = pages per consumer iteration: 2 amortises the softmax reduction and
+// gives more independent work, but needs registers the 168-register
+// single-n-tile configuration does not have.
+template <int KVDT, int NTW, int RG, int NW, int QS = 0, int NP = (NTW > 1 ? 2 : 1)>
 int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
-  using P = Plan<KVDT, NTW, RG, NW>;
-  auto kern = paged_decode_kernel<KVDT, NTW, RG, NW>;
+  using P = Plan<KVDT, NTW, RG, NW, QS>;
+  auto kern = paged_decode_kernel<KVDT, NTW, RG, NW, QS, NP>;
   static bool configured = false;  // attribute set once per process (idempotent)
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kDynamicBytes) !=
@@ -860,7 +964,12 @@ int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
   // two or more stages; bf16 stages are 16 KiB, so fewer streams share the
   // 13 that fit and each still double-buffers.
   constexpr bool fp4 = KVDT == PNKV_KV_NVFP4;
-  if (rows <= 8) return launch_decode<KVDT, 1, 1, fp4 ? 12 : 7>(map, a, grid, stream);
+#ifndef PNKV_NVFP4_NW
+#define PNKV_NVFP4_NW 12
+#define PNKV_NVFP4_QS 0
+#endif
+  if (rows <= 8)
+    return launch_decode<KVDT, 1, 1, fp4 ? PNKV_NVFP4_NW : 7, fp4 ? PNKV_NVFP4_QS : 0>(map, a, grid, stream);
   if (rows <= 16) return launch_decode<KVDT, 2, 1, 7>(map, a, grid, stream);
   if (rows <= 32) return launch_decode<KVDT, 2, 2, 7>(map, a, grid, stream);
   if (rows <= 64) return launch_decode<KVDT, 2, 4, 5>(map, a, grid, stream);

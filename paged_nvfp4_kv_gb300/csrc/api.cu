@@ -2,6 +2,9 @@
 // and the per-device SM count cache.
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "host_common.h"
 
 namespace pnkv {
@@ -27,6 +30,37 @@ int device_sm_count(int* out_sms) {
     return PNKV_ERR_CUDA;
   *out_sms = sms;
   return PNKV_OK;
+}
+
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// The pool seen as a 2-D byte tensor [num_pages * hkv * box_rows][128].
+int make_pool_map(const pnkv_cache* c, int box_rows, void* map_out) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return PNKV_ERR_CUDA;
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * box_rows;
+  if (rows >= (1ull << 31)) return PNKV_ERR_INVALID_ARG;  // TMA row coordinates are int32
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->pool, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PNKV_OK : PNKV_ERR_CUDA;
 }
 
 }  // namespace pnkv

@@ -39,6 +39,13 @@
 #include "host_common.h"
 
 namespace pnkv {
+
+int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32_t* qo_indptr,
+                   const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                   int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal, float* o_part,
+                   float* lse_part, int64_t part_slots, int32_t* work_meta, int32_t* dev_err,
+                   cudaStream_t stream);
+
 namespace {
 
 // A CTA has NW warps: the last one produces, the consumers are the largest
@@ -392,10 +399,10 @@ __device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const Q& qf, flo
       const uint32_t sh = (blk < 2) ? shi01 : shi23;
       const uint32_t sel = (blk & 1) ? 0x3232u : 0x1010u;
       const uint32_t scl = prmt(sl, sl, sel), sch = prmt(sh, sh, sel);
-#pragma unroll
       uint32_t cl[4], ch[4];
       e2m1x8_unpack(wl[q], cl);
       e2m1x8_unpack(wh[q], ch);
+#pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int kk = 8 * h + 2 * q + half;
         uint32_t af[4];
@@ -911,35 +918,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
 // ---------------------------------------------------------------------------
 // Host side.
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// The pool seen as a 2-D byte tensor [num_pages * hkv * box_rows][128].
-int make_pool_map(const pnkv_cache* c, int box_rows, CUtensorMap* map) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
-  if (!enc) return PNKV_ERR_CUDA;
-  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * box_rows;
-  if (rows >= (1ull << 31)) return PNKV_ERR_INVALID_ARG;  // TMA row coordinates are int32
-  const cuuint64_t dims[2] = {128, rows};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->pool, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PNKV_OK : PNKV_ERR_CUDA;
-}
-
 // NP = pages per consumer iteration: 2 amortises the softmax reduction and
 // gives more independent work, but needs registers the 168-register
 // single-n-tile configuration does not have.
@@ -988,6 +966,10 @@ extern "C" int64_t pnkv_decode_slots(const pnkv_cache* cache, int32_t batch, int
   if (st != PNKV_OK) return st;
   if (batch < 1 || max_qlen < 1 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
     return PNKV_ERR_INVALID_ARG;
+  // the tensor-core tile path (more than 64 rows per KV head) writes one slot
+  // per (sequence, KV head); the split-KV path one per piece
+  if (static_cast<int64_t>(num_q_heads / cache->num_kv_heads) * max_qlen > 64)
+    return static_cast<int64_t>(batch) * cache->num_kv_heads;
   int grid = 0;
   if ((st = decode_grid(&grid)) != PNKV_OK) return st;
   return static_cast<int64_t>(batch) * cache->num_kv_heads + grid;
@@ -1017,10 +999,13 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   const int group = num_q_heads / cache->num_kv_heads;
   if (group > 8) return PNKV_ERR_UNSUPPORTED;
   const int64_t rows_per_slot = static_cast<int64_t>(group) * max_qlen;
+  if (rows_per_slot > 64)  // many query rows per KV head: the tensor-core tile path
+    return launch_prefill(cache, q_roped, qo_indptr, page_table, pt_stride, seq_lens, batch, num_q_heads,
+                          max_qlen, sm_scale, causal, o_part, lse_part, part_slots, work_meta, dev_err,
+                          as_stream(stream));
   int grid = 0;
   if ((st = decode_grid(&grid)) != PNKV_OK) return st;
   if (part_slots < static_cast<int64_t>(batch) * cache->num_kv_heads + grid) return PNKV_ERR_INVALID_ARG;
-  if (rows_per_slot > 64) return PNKV_ERR_UNSUPPORTED;
 
   DecodeArgs a;
   a.num_pages = cache->num_pages;

@@ -45,6 +45,11 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 // SM count of the current device (cached per device id).
 int device_sm_count(int* out_sms);
 
+// The pool as a 2-D byte tensor [num_pages * num_kv_heads * box_rows][128]
+// with a box of box_rows x 128 bytes and 128-byte swizzling (one head record
+// of a page per box); written to *map (a CUtensorMap).
+int make_pool_map(const pnkv_cache* c, int box_rows, void* map);
+
 // Pool geometry checks shared by every call that touches the pool.
 inline int check_cache(const pnkv_cache* c) {
   if (!c || !c->pool || c->num_pages <= 0 || c->page_size != 16 || c->head_dim != 256 ||

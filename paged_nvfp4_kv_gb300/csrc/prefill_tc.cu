@@ -1,0 +1,692 @@
+// Chunked-prefill attention tile on the 5th-generation tensor cores
+// (tcgen05 MMAs with TMEM accumulators), used by paged_decode_attention when a
+// KV head has more query rows than the register-tile decode path handles.
+//
+// Same attention as the decode path: for every query row, softmax(q k^T *
+// sm_scale) v over its visible keys (causal inside the chunk: query token t
+// of a chunk of qlen tokens at the end of a sequence of len keys sees keys
+// 0 .. len - qlen + t).  The chunk is prefilled against the paged NVFP4 cache
+// ("A 1,048,576-token context on two RTX 5090s", section "Against vLLM:
+// prefill loses, decode wins, and one surprise": prompts are ingested in
+// chunks, 1,024 tokens in one engine and 16,768 batched tokens in the other).
+//
+// A CTA tile is 128 TMEM lanes = 128 query rows of one KV head: T = 128 / G
+// consecutive query tokens times the G query heads that share the KV head
+// (GQA), so every KV byte read serves all G heads.  Keys are swept in
+// blocks of 32 (two 16-token pages):
+//   producer warp   TMA-loads the two pages' NVFP4 head records (raw ring)
+//   dequant warps   widen K to fp16 [32 keys][256 dims] and V to fp16
+//                   V^T [256 dims][32 keys] (E2M1 x E4M3 is exact in fp16),
+//                   both in the no-swizzle K-major core-matrix layout
+//   MMA thread      S = Q K^T   (M 128, N 32, K 256)  -> TMEM, double buffer
+//                   O += P V    (M 128, N 256, K 32)  -> TMEM
+//   softmax warps   one row per thread: tcgen05.ld of S, online softmax,
+//                   P (fp16) -> shared memory; O is rescaled in TMEM only when
+//                   a row's running maximum grows by more than 2^8, so the
+//                   exponentials stay below 256 and most blocks need no
+//                   rescale (the final normalisation divides by the sum of
+//                   the same fp16 values that entered P V)
+// Per-tensor K/V scales fold into the logit scale and the output, as in the
+// decode path.  The CTA writes one normalised partial (with its natural-log
+// LSE) per row into the (sequence, KV head) slot, which split_kv_combine
+// passes through.
+#include <cmath>
+
+#include <cudaTypedefs.h>
+
+#include "device_common.cuh"
+#include "host_common.h"
+
+namespace pnkv {
+namespace {
+
+constexpr int kThreads = 320;         // 10 warps
+// warps 0-3 run the softmax, one TMEM lane quarter (32 rows) each
+constexpr int kDequantWarp0 = 4;      // warps 4-7
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBlockKeys = 32;        // keys per KV block (two pages)
+constexpr int kRawStages = 4;
+constexpr int kRawPageBytes = 5120;   // 4,608-byte record, 1,024-aligned slot
+constexpr int kRawStageBytes = 2 * kRawPageBytes;
+constexpr uint32_t kRecBytes = 4608;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
+
+// Shared memory plan (offsets from a 1,024-byte aligned base).
+constexpr int kQOff = 0;                                  // 128 x 256 fp16
+constexpr int kQBytes = 128 * 256 * 2;
+constexpr int kKOff = kQOff + kQBytes;                    // 2 x [32 x 256] fp16
+constexpr int kKBytes = kBlockKeys * 256 * 2;
+constexpr int kVOff = kKOff + 2 * kKBytes;                // 2 x [256 x 32] fp16
+constexpr int kVBytes = 256 * kBlockKeys * 2;
+constexpr int kPOff = kVOff + 2 * kVBytes;                // 2 x [128 x 32] fp16
+constexpr int kPBytes = 128 * kBlockKeys * 2;
+constexpr int kRawOff = kPOff + 2 * kPBytes;              // raw NVFP4 records
+constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
+// barriers: raw_full[4], raw_empty[4], kv_full[2], kv_free[2], s_full[2],
+// s_free[2], p_full[2], pv_done[2], q_full, final
+constexpr int kNumBars = 4 + 4 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort, raw valid[4]
+constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+static_assert(kSmemBytes <= 232448, "prefill shared memory plan too large");
+
+// TMEM columns: S double buffer at 0 and 32, O at 64 .. 319.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 64;
+
+struct PrefillArgs {
+  int64_t num_pages;
+  int32_t hkv, group, tpt;  // tpt: query tokens per tile (128 / group)
+  float qk_scale_log2, out_scale;
+  const uint16_t* q;
+  const int32_t* qo_indptr;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  const int32_t* seq_lens;
+  int32_t batch, hq, max_qlen, rows_per_slot, causal;
+  float* o_part;
+  float* lse_part;
+  int64_t part_slots;
+  int32_t* work_meta;
+  int32_t* dev_err;
+};
+
+// ------------------------------------------------------------ tcgen05 --
+// Byte offset of element (r, k) in a no-swizzle K-major tile whose rows hold
+// kdim 16-bit elements: 8 x 8 core matrices of 128 contiguous bytes, the core
+// matrices of a row group consecutive along K.
+__device__ __forceinline__ uint32_t core_off(uint32_t r, uint32_t k, uint32_t kdim) {
+  return (((r >> 3) * (kdim >> 3) + (k >> 3)) << 7) + ((r & 7) << 4) + ((k & 7) << 1);
+}
+
+// Shared-memory matrix descriptor: start address, leading-dimension byte
+// offset (between core matrices along K), stride-dimension byte offset
+// (between 8-row groups), descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 16 consecutive TMEM columns of this warp's 32 lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// --------------------------------------------------------------- tiles --
+// Tiles enumerate (sequence, KV head, token tile); every role of a CTA walks
+// the same list: tile = blockIdx.x + k * gridDim.x.
+struct Tile {
+  int b, h;
+  int t0, ntok;      // first query token (within the chunk) and tokens in tile
+  int q0, qlen, len; // qo_indptr[b], chunk length, keys of the sequence
+  int nblocks;       // key blocks the tile needs
+  int keys;          // keys the last row of the tile may see
+};
+
+__device__ __forceinline__ bool seq_ok(const PrefillArgs& a, int b, int* q0, int* qlen, int* len) {
+  *len = __ldg(a.seq_lens + b);
+  *q0 = __ldg(a.qo_indptr + b);
+  *qlen = __ldg(a.qo_indptr + b + 1) - *q0;
+  return *qlen > 0 && *qlen <= a.max_qlen && *qlen <= *len && *q0 >= 0 &&
+         static_cast<int64_t>((*len + 15) >> 4) <= a.pt_stride;
+}
+
+// The idx-th tile, or false if there is none.
+__device__ bool find_tile(const PrefillArgs& a, int64_t idx, Tile* t) {
+  int64_t base = 0;
+  for (int b = 0; b < a.batch; ++b) {
+    int q0, qlen, len;
+    if (!seq_ok(a, b, &q0, &qlen, &len)) continue;
+    const int per_head = (qlen + a.tpt - 1) / a.tpt;
+    const int64_t n = static_cast<int64_t>(per_head) * a.hkv;
+    if (idx < base + n) {
+      const int64_t r = idx - base;
+      t->b = b;
+      t->h = static_cast<int>(r / per_head);
+      const int tt = static_cast<int>(r % per_head);
+      t->t0 = tt * a.tpt;
+      t->ntok = min(a.tpt, qlen - t->t0);
+      t->q0 = q0;
+      t->qlen = qlen;
+      t->len = len;
+      t->keys = a.causal ? len - qlen + t->t0 + t->ntok : len;
+      t->nblocks = (t->keys + kBlockKeys - 1) / kBlockKeys;
+      return true;
+    }
+    base += n;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint64_t* bar_at(uint8_t* smem, int i) {
+  return reinterpret_cast<uint64_t*>(smem + kBarOff) + i;
+}
+enum {
+  B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_KV_FULL = 8, B_KV_FREE = 10, B_S_FULL = 12, B_S_FREE = 14,
+  B_P_FULL = 16, B_PV_DONE = 18, B_Q_FULL = 20, B_FINAL = 21
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  volatile uint32_t* abort_flag = misc + 1;
+  uint32_t* raw_valid = misc + 2;  // [kRawStages] bit 0/1: page 0/1 loaded
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar_at(smem, B_RAW_FULL + i), 1);
+      mbar_init(bar_at(smem, B_RAW_EMPTY + i), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_at(smem, B_KV_FULL + i), 4);
+      mbar_init(bar_at(smem, B_KV_FREE + i), 1);
+      mbar_init(bar_at(smem, B_S_FULL + i), 1);
+      mbar_init(bar_at(smem, B_S_FREE + i), 4);
+      mbar_init(bar_at(smem, B_P_FULL + i), 4);
+      mbar_init(bar_at(smem, B_PV_DONE + i), 1);
+    }
+    mbar_init(bar_at(smem, B_Q_FULL), 4);
+    mbar_init(bar_at(smem, B_FINAL), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(misc)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  griddep_wait();
+  griddep_launch_dependents();
+
+  auto fail = [&]() {
+    flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+  // single-thread wait (the MMA issuer, producer lane 0)
+  auto wait = [&](int bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (!mbar_wait(bar_at(smem, bar), parity)) {
+      fail();
+      return false;
+    }
+    return true;
+  };
+  // warp-uniform wait: every lane waits, the warp agrees on the outcome, so
+  // an abort never splits a warp before a collective operation
+  auto wait_warp = [&](int bar, uint32_t parity) -> bool {
+    bool ok = !*abort_flag && mbar_wait(bar_at(smem, bar), parity);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) fail();
+    return ok;
+  };
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------- producer
+    const uint64_t policy = l2_policy_evict_first();
+    int64_t gb = 0;
+    bool ok = true;
+    Tile t;
+    for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x) {
+      const int32_t* row = a.page_table + static_cast<int64_t>(t.b) * a.pt_stride;
+      const int pages = (t.len + 15) >> 4;
+      for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
+        const int rs = static_cast<int>(gb % kRawStages);
+        if (lane == 0) ok = wait(B_RAW_EMPTY + rs, static_cast<uint32_t>((gb / kRawStages) & 1) ^ 1u);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // lanes 0 and 1: the block's two pages
+        int32_t page = -1;
+        bool in_seq = false;
+        if (lane < 2) {
+          const int pi = 2 * j + lane;
+          in_seq = pi < pages;
+          if (in_seq) {
+            page = __ldg(row + pi);
+            if (page < 0 || page >= a.num_pages) {
+              flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
+              page = -1;
+            }
+          }
+        }
+        const unsigned load = __ballot_sync(0xffffffffu, lane < 2 && page >= 0);
+        if (lane == 0) {
+          raw_valid[rs] = load;
+          mbar_arrive_expect_tx(bar_at(smem, B_RAW_FULL + rs), __popc(load) * kRecBytes);
+        }
+        __syncwarp();
+        if (lane < 2 && page >= 0) {
+          const int32_t y = (page * a.hkv + t.h) * 36;
+          tma_load_2d(smem + kRawOff + rs * kRawStageBytes + lane * kRawPageBytes, &tmap, 0, y,
+                      bar_at(smem, B_RAW_FULL + rs), policy);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // bounded drain of the loads that may still be landing
+      const int64_t first = gb > kRawStages ? gb - kRawStages : 0;
+      for (int64_t i = first; i < gb; ++i)
+        mbar_wait(bar_at(smem, B_RAW_FULL + static_cast<int>(i % kRawStages)),
+                  static_cast<uint32_t>((i / kRawStages) & 1));
+    }
+  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + 4) {
+    // ----------------------------------------------------------- dequant
+    const int dt = threadIdx.x - kDequantWarp0 * 32;  // 0..127
+    int64_t gb = 0;
+    bool ok = true;
+    Tile t;
+    for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x) {
+      for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
+        const int rs = static_cast<int>(gb % kRawStages);
+        const int kb = static_cast<int>(gb & 1);
+        ok = wait_warp(B_RAW_FULL + rs, static_cast<uint32_t>((gb / kRawStages) & 1));
+        if (ok && gb >= 2) ok = wait_warp(B_KV_FREE + kb, static_cast<uint32_t>(((gb - 2) >> 1) & 1));
+        if (!ok) break;
+        const uint32_t valid = raw_valid[rs];
+        const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStageBytes);
+        uint8_t* ktile = smem + kKOff + kb * kKBytes;
+        uint8_t* vtile = smem + kVOff + kb * kVBytes;
+        // K: 512 units (key, 16-dim block), 4 per thread
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int u = dt + 128 * i;
+          const int key = u >> 4, blk = u & 15;
+          const int pg = key >> 4, slot = key & 15;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if ((valid >> pg) & 1) {
+            const uint32_t rec = raw + pg * kRawPageBytes;
+            uint2 w;
+            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w.x), "=r"(w.y) : "r"(rec + swz128(slot, 8 * blk)));
+            const uint32_t sbyte = lds8(rec + swz128(16 + (slot >> 3), (slot & 7) * 16 + blk));
+            uint32_t s2 = e4m3x2_to_f16x2(sbyte);
+            s2 = prmt(s2, s2, 0x1010u);
+            uint32_t c0[4], c1[4];
+            e2m1x8_unpack(w.x, c0);
+            e2m1x8_unpack(w.y, c1);
+            lo = make_uint4(hmul2(c0[0], s2), hmul2(c0[1], s2), hmul2(c0[2], s2), hmul2(c0[3], s2));
+            hi = make_uint4(hmul2(c1[0], s2), hmul2(c1[1], s2), hmul2(c1[2], s2), hmul2(c1[3], s2));
+          }
+          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk, 256)) = lo;
+          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk + 8, 256)) = hi;
+        }
+        // V^T: 1,024 units (dim d, 8 keys), 8 per thread
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+          const int u = dt + 128 * i;
+          const int d = u >> 2, c = u & 3;
+          const int pg = c >> 1;             // page of keys 8c .. 8c+7
+          const int p0 = 4 * (c & 1);        // first slot pair in the page
+          uint4 out = make_uint4(0, 0, 0, 0);
+          if ((valid >> pg) & 1) {
+            const uint32_t rec = raw + pg * kRawPageBytes;
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int pr = p0 + q;  // slot pair: slots 2pr, 2pr+1
+              const uint32_t code = lds8(rec + swz128(18 + 2 * pr + (d >> 7), d & 127));
+              const int s0 = 2 * pr, s1 = 2 * pr + 1;
+              const uint32_t sc0 = lds8(rec + swz128(34 + (s0 >> 3), (s0 & 7) * 16 + (d >> 4)));
+              const uint32_t sc1 = lds8(rec + swz128(34 + (s1 >> 3), (s1 & 7) * 16 + (d >> 4)));
+              uint32_t cv;
+              asm("{ .reg .b8 t; .reg .b16 w; cvt.u16.u32 w, %1; cvt.u8.u16 t, w; cvt.rn.f16x2.e2m1x2 %0, t; }"
+                  : "=r"(cv)
+                  : "r"(code));
+              o[q] = hmul2(cv, e4m3x2_to_f16x2(sc0 | (sc1 << 8)));
+            }
+            out = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+          *reinterpret_cast<uint4*>(vtile + core_off(d, 8 * c, kBlockKeys)) = out;
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_at(smem, B_KV_FULL + kb));
+          mbar_arrive(bar_at(smem, B_RAW_EMPTY + rs));
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t q_base = smem_addr(smem + kQOff);
+      const uint32_t idesc_qk = idesc_f16(128, kBlockKeys);
+      const uint32_t idesc_pv = idesc_f16(128, 256);
+      int64_t gb = 0;     // next block whose QK is issued
+      int64_t tcount = 0;
+      bool ok = true, issued_any = false;
+      Tile t;
+      auto issue_qk = [&](int64_t g) -> bool {
+        const int kb = static_cast<int>(g & 1), sb = static_cast<int>(g & 1);
+        if (!wait(B_KV_FULL + kb, static_cast<uint32_t>((g >> 1) & 1))) return false;
+        if (g >= 2 && !wait(B_S_FREE + sb, static_cast<uint32_t>(((g - 2) >> 1) & 1))) return false;
+        tc_fence_after();
+        const uint32_t k_base = smem_addr(smem + kKOff + kb * kKBytes);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          umma_f16(tmem + kTmemS + sb * kBlockKeys, smem_desc(q_base + kk * 256, 128, 4096),
+                   smem_desc(k_base + kk * 256, 128, 4096), idesc_qk, kk > 0);
+        umma_commit(bar_at(smem, B_S_FULL + sb));
+        issued_any = true;
+        return true;
+      };
+      for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x, ++tcount) {
+        ok = wait(B_Q_FULL, static_cast<uint32_t>(tcount & 1));
+        if (!ok) break;
+        const int64_t g0 = gb;
+        ok = issue_qk(g0);
+        for (int j = 0; ok && j < t.nblocks; ++j) {
+          const int64_t g = g0 + j;
+          if (j + 1 < t.nblocks) {
+            ok = issue_qk(g + 1);
+            if (!ok) break;
+          }
+          const int pb = static_cast<int>(g & 1), kb = static_cast<int>(g & 1);
+          ok = wait(B_P_FULL + pb, static_cast<uint32_t>((g >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t p_base = smem_addr(smem + kPOff + pb * kPBytes);
+          const uint32_t v_base = smem_addr(smem + kVOff + kb * kVBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+            umma_f16(tmem + kTmemO, smem_desc(p_base + kk * 256, 128, 512), smem_desc(v_base + kk * 256, 128, 512),
+                     idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar_at(smem, B_KV_FREE + kb));
+          umma_commit(bar_at(smem, B_PV_DONE + pb));
+        }
+        gb = g0 + t.nblocks;
+      }
+      // every issued MMA completes before TMEM is released
+      if (issued_any) {
+        umma_commit(bar_at(smem, B_FINAL));
+        mbar_wait(bar_at(smem, B_FINAL), 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- softmax
+    const int r = threadIdx.x;  // row = TMEM lane (warps 0-3)
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    int64_t gb = 0;
+    int64_t tcount = 0;
+    bool ok = true;
+    Tile t;
+    for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x, ++tcount) {
+      const int tok = t.t0 + r / a.group;
+      const int head = r % a.group;
+      const bool row_live = r < a.tpt * a.group && r / a.group < t.ntok;
+      const int lim = !row_live ? 0 : (a.causal ? t.len - t.qlen + tok + 1 : t.len);
+      // Q row -> fp16, core-matrix layout (the previous tile's MMAs are done:
+      // its epilogue waited for the last P V)
+      {
+        uint8_t* qt = smem + kQOff;
+        const uint4* src = row_live ? reinterpret_cast<const uint4*>(
+                                          a.q + (static_cast<int64_t>(t.q0 + tok) * a.hq + t.h * a.group + head) * 256)
+                                    : nullptr;
+#pragma unroll 4
+        for (int c = 0; c < 32; ++c) {
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (row_live) {
+            const uint4 w = __ldg(src + c);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              h[e] = f32x2_to_f16x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xFFFF0000u));
+            o = make_uint4(h[0], h[1], h[2], h[3]);
+          }
+          *reinterpret_cast<uint4*>(qt + core_off(r, 8 * c, 256)) = o;
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(smem, B_Q_FULL));
+      }
+      float m_used = -INFINITY, l = 0.f;
+      const int64_t g0 = gb;
+      for (int j = 0; j < t.nblocks; ++j) {
+        const int64_t g = g0 + j;
+        const int sb = static_cast<int>(g & 1), pb = static_cast<int>(g & 1);
+        ok = wait_warp(B_S_FULL + sb, static_cast<uint32_t>((g >> 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[32];
+        {
+          uint32_t x0[16], x1[16];
+          tmem_ld16(lane_addr + kTmemS + sb * kBlockKeys, x0);
+          tmem_ld16(lane_addr + kTmemS + sb * kBlockKeys + 16, x1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            sr[e] = x0[e];
+            sr[16 + e] = x1[e];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(smem, B_S_FREE + sb));
+        float sv[32];
+        float mb = -INFINITY;
+        const int key0 = j * kBlockKeys;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float z = __uint_as_float(sr[k]) * a.qk_scale_log2;
+          sv[k] = (key0 + k < lim) ? z : -INFINITY;
+          mb = fmaxf(mb, sv[k]);
+        }
+        // lazy rescale: move the exponent base only when the row max grows
+        // by more than the threshold (or for the first finite max)
+        float alpha = 1.f;
+        bool move = mb > m_used + kRescaleThreshold || (m_used == -INFINITY && mb > -INFINITY);
+        float base_new = move ? mb : m_used;
+        if (move && m_used != -INFINITY) alpha = fast_exp2(m_used - base_new);
+        // O holds this row's sum so far only after at least one P V
+        const bool need = move && m_used != -INFINITY && j > 0;
+        if (__any_sync(0xffffffffu, need)) {
+          ok = wait_warp(B_PV_DONE + static_cast<int>((g - 1) & 1), static_cast<uint32_t>(((g - 1) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const float f = need ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 256; c += 16) {
+            uint32_t x[16];
+            tmem_ld16(lane_addr + kTmemO + c, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * f);
+            tmem_st16(lane_addr + kTmemO + c, x);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        l *= alpha;
+        m_used = base_new;
+        const float bse = (m_used == -INFINITY) ? 0.f : m_used;
+        uint32_t ph[16];
+        float add = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          ph[k] = f32x2_to_f16x2(fast_exp2(sv[2 * k] - bse), fast_exp2(sv[2 * k + 1] - bse));
+          const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&ph[k]));
+          add += f2.x + f2.y;
+        }
+        l += add;
+        // P buffer pb was last read by the P V of block g - 2
+        if (g >= 2) {
+          ok = wait_warp(B_PV_DONE + pb, static_cast<uint32_t>(((g - 2) >> 1) & 1));
+          if (!ok) break;
+        }
+        uint8_t* pt = smem + kPOff + pb * kPBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
+              make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(smem, B_P_FULL + pb));
+      }
+      if (!ok) break;
+      gb = g0 + t.nblocks;
+      // epilogue: final O row, normalised, into the (sequence, KV head) slot
+      const int64_t gl = gb - 1;
+      ok = wait_warp(B_PV_DONE + static_cast<int>(gl & 1), static_cast<uint32_t>((gl >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t seg = static_cast<int64_t>(t.b) * a.hkv + t.h;
+      const int64_t n = static_cast<int64_t>(tok) * a.group + head;
+      const float inv = l > 0.f ? a.out_scale / l : 0.f;
+      float* dst = a.o_part + (seg * a.rows_per_slot + n) * 256;
+      const bool write = row_live && seg < a.part_slots && n < a.rows_per_slot;
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 16) {
+        uint32_t x[16];
+        tmem_ld16(lane_addr + kTmemO + c, x);
+        tmem_wait_ld();
+        if (write) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(dst + c + e) =
+                make_float4(__uint_as_float(x[e]) * inv, __uint_as_float(x[e + 1]) * inv,
+                            __uint_as_float(x[e + 2]) * inv, __uint_as_float(x[e + 3]) * inv);
+        }
+      }
+      tc_fence_before();
+      if (write) a.lse_part[seg * a.rows_per_slot + n] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (r == 0 && t.t0 == 0) {
+        a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg);
+        a.work_meta[4 + 2 * seg + 1] = 1;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// Work metadata header and empty segments (sequences without query rows).
+__global__ void prefill_meta_kernel(const PrefillArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    a.work_meta[0] = a.hkv;
+    a.work_meta[1] = a.group;
+    a.work_meta[2] = a.rows_per_slot;
+    a.work_meta[3] = a.batch;
+  }
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.batch; b += gridDim.x * blockDim.x) {
+    int q0, qlen, len;
+    if (!seq_ok(a, b, &q0, &qlen, &len)) {
+      if (__ldg(a.qo_indptr + b + 1) - __ldg(a.qo_indptr + b) != 0)
+        flag_error(a.dev_err, PNKV_DEV_ERR_QO_INDPTR);
+      for (int h = 0; h < a.hkv; ++h) {
+        a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h)] = 0;
+        a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h) + 1] = 0;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// Launch the tensor-core tile path (called by paged_decode_attention when a KV
+// head has more than 64 query rows).
+int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32_t* qo_indptr,
+                   const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                   int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal, float* o_part,
+                   float* lse_part, int64_t part_slots, int32_t* work_meta, int32_t* dev_err,
+                   cudaStream_t stream) {
+  if (cache->dtype != PNKV_KV_NVFP4) return PNKV_ERR_UNSUPPORTED;
+  PrefillArgs a;
+  a.num_pages = cache->num_pages;
+  a.hkv = cache->num_kv_heads;
+  a.group = num_q_heads / cache->num_kv_heads;
+  a.tpt = 128 / a.group;
+  a.qk_scale_log2 = sm_scale * cache->k_scale * kLog2e;
+  a.out_scale = cache->v_scale;
+  a.q = q_roped;
+  a.qo_indptr = qo_indptr;
+  a.page_table = page_table;
+  a.pt_stride = pt_stride;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.hq = num_q_heads;
+  a.max_qlen = max_qlen;
+  a.rows_per_slot = a.group * max_qlen;
+  a.causal = causal ? 1 : 0;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.part_slots = part_slots;
+  a.work_meta = work_meta;
+  a.dev_err = dev_err;
+  if (part_slots < static_cast<int64_t>(batch) * a.hkv) return PNKV_ERR_INVALID_ARG;
+  CUtensorMap map;
+  int st = make_pool_map(cache, 36, &map);
+  if (st != PNKV_OK) return st;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != PNKV_OK) return st;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(prefill_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return PNKV_ERR_CUDA;
+    configured = true;
+  }
+  st = launch_pdl(prefill_meta_kernel, dim3((batch + 255) / 256), dim3(256), 0, stream, a);
+  if (st != PNKV_OK) return st;
+  return launch_pdl(prefill_tile_kernel, dim3(sms), dim3(kThreads), kSmemBytes, stream, map, a);
+}
+
+}  // namespace pnkv

@@ -64,6 +64,9 @@ CASES = {
     "long-nvfp4": ("nvfp4", [70000, 7000], [1, 1]),
     "long-verify5-nvfp4": ("nvfp4", [40000, 23000], [5, 5]),
     "long-verify5-bf16": ("bf16", [30000], [5]),
+    # more than 64 query rows per KV head: the tensor-core tile path
+    "prefill-nvfp4": ("nvfp4", [3000, 500, 77], [100, 37, 1]),
+    "prefill-long-nvfp4": ("nvfp4", [40000], [300]),
 }
 
 

@@ -138,6 +138,30 @@ def profiled_traffic(kv_dtype):
     return int(vals["traffic_bytes_per_launch:"])
 
 
+def attention_flops(w):
+    """QK^T + PV FLOPs of one step: every query row times its visible keys
+    times head dim x 2 (multiply-add) x 2 (two products)."""
+    tot = 0
+    for b in range(w.batch):
+        n, nq = int(w.seq_lens[b]), int(w.qlen[b])
+        vis = (n - nq) * nq + nq * (nq + 1) // 2 if w.causal else n * nq
+        tot += vis * w.num_q_heads
+    return tot * w.head_dim * 4
+
+
+def tensor_peak():
+    """fp16/bf16 dense tensor peak in TFLOP/s (sustained figure: the tile
+    kernel runs for most of a second)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("bf16_tflops_sustained", "bf16_tflops"):
+            if key in d:
+                return float(d[key]), "measured"
+    return 1700.0, "fallback"
+
+
 def workload(cfg):
     from paged_nvfp4_kv_gb300 import workloads as W
     return W.CONFIGS[cfg]()
@@ -328,6 +352,19 @@ def run_ours(args):
     peak, peak_kind = peaks()
     algo_bytes = keys * ALGO_BYTES_PER_TOKEN[w.kv_dtype]
     achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(w.kv_dtype),
+                "peak_kind": peak_kind, "kernel": "paged_decode_attention",
+                "algorithmic_bytes_per_launch": algo_bytes}
+    if int(w.total_q) * w.num_q_heads // w.num_kv_heads > 64 * w.batch:
+        # the tensor-core tile path: a dense contraction, judged against the
+        # tensor peak (QK^T and PV, 2 FLOP per multiply-add, causal-exact)
+        flops = attention_flops(w)
+        tflops = flops / (decode_ms * 1e-3) / 1e12
+        tpeak, tkind = tensor_peak()
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": tflops / tpeak, "traffic": None, "peak_kind": tkind,
+                    "kernel": "prefill_tile_kernel (tcgen05)", "algorithmic_flops_per_launch": flops}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -340,11 +377,7 @@ def run_ours(args):
         "kernels_ms": {"kv_append_nvfp4": append_ms, "paged_decode_attention": decode_ms,
                        "split_kv_combine": combine_ms},
         "hbm_gbs_decode": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.kv_dtype),
-                     "peak_kind": peak_kind,
-                     "kernel": "paged_decode_attention",
-                     "algorithmic_bytes_per_launch": algo_bytes},
+        "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 3 * K,

@@ -53,7 +53,10 @@ namespace {
 // to 8 warps (256 threads) keep 255 registers per thread and 12 warps (384)
 // keep 168: the single-n-tile NVFP4 path fits 168 and runs 11 consumers; the
 // other paths need the larger budget and run with at most 8 warps.
-constexpr int kIssueLanes = 8;  // producer lanes that issue TMA loads together
+#ifndef PNKV_ISSUE_LANES
+#define PNKV_ISSUE_LANES 8
+#endif
+constexpr int kIssueLanes = PNKV_ISSUE_LANES;  // producer lanes that issue TMA loads together
 template <int NW, int RG>
 struct Consumers {
   static constexpr int kWarps = ((NW - 1) / RG) * RG;
@@ -261,7 +264,9 @@ struct Plan {
   static constexpr int kDynamicBytes = kTotal + 1024;          // room to align the base
   static_assert(kStages >= 2 * kStreams, "every consumer stream needs two stages");
   static_assert(kStages % kStreams == 0, "stages must split evenly over the streams");
-  static_assert(kStages >= kIssueLanes, "lanes that issue together need distinct stages");
+  // producer lanes that issue together (they need distinct stages)
+  static constexpr int kIssue = kIssueLanes <= kStages ? kIssueLanes : 8;
+  static_assert(kStages >= kIssue && 32 % kIssue == 0, "lanes that issue together need distinct stages");
   static_assert(kDynamicBytes <= kMaxSmem, "shared memory plan too large");
 };
 
@@ -679,8 +684,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
         const int32_t page = mine ? __ldg(row + j0 + lane) : 0;
         bool lane_ok = true;
 #pragma unroll 1
-        for (int g = 0; g < 32 / kIssueLanes; ++g) {
-          if (mine && lane / kIssueLanes == g) {
+        for (int g = 0; g < 32 / P::kIssue; ++g) {
+          if (mine && lane / P::kIssue == g) {
             const int64_t i = issued + lane;
             const int s = static_cast<int>(i % P::kStages);
             const uint32_t par = static_cast<uint32_t>((i / P::kStages) & 1) ^ 1u;

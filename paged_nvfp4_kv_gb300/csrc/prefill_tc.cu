@@ -40,13 +40,21 @@
 namespace pnkv {
 namespace {
 
-constexpr int kThreads = 320;         // 10 warps
+constexpr int kThreads = 448;         // 14 warps
 // warps 0-3 run the softmax, one TMEM lane quarter (32 rows) each
-constexpr int kDequantWarp0 = 4;      // warps 4-7
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kDequantWarp0 = 4;      // warps 4-11
+constexpr int kDequantWarps = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr int kBlockKeys = 32;        // keys per KV block (two pages)
-constexpr int kRawStages = 4;
+// ring depths: QK runs up to kSStages - 1 blocks ahead of P V, so the softmax
+// of a block overlaps the tensor work of the next ones
+constexpr int kRawStages = 2;
+constexpr int kKStages = 4;
+constexpr int kVStages = 3;
+constexpr int kSStages = 4;
+constexpr int kPStages = 3;
+constexpr int kLookahead = kSStages - 1;
 constexpr int kRawPageBytes = 5120;   // 4,608-byte record, 1,024-aligned slot
 constexpr int kRawStageBytes = 2 * kRawPageBytes;
 constexpr uint32_t kRecBytes = 4608;
@@ -57,25 +65,38 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 // Shared memory plan (offsets from a 1,024-byte aligned base).
 constexpr int kQOff = 0;                                  // 128 x 256 fp16
 constexpr int kQBytes = 128 * 256 * 2;
-constexpr int kKOff = kQOff + kQBytes;                    // 2 x [32 x 256] fp16
+constexpr int kKOff = kQOff + kQBytes;                    // ring of [32 x 256] fp16
 constexpr int kKBytes = kBlockKeys * 256 * 2;
-constexpr int kVOff = kKOff + 2 * kKBytes;                // 2 x [256 x 32] fp16
+constexpr int kVOff = kKOff + kKStages * kKBytes;         // ring of [256 x 32] fp16
 constexpr int kVBytes = 256 * kBlockKeys * 2;
-constexpr int kPOff = kVOff + 2 * kVBytes;                // 2 x [128 x 32] fp16
+constexpr int kPOff = kVOff + kVStages * kVBytes;         // ring of [128 x 32] fp16
 constexpr int kPBytes = 128 * kBlockKeys * 2;
-constexpr int kRawOff = kPOff + 2 * kPBytes;              // raw NVFP4 records
+constexpr int kRawOff = kPOff + kPStages * kPBytes;       // raw NVFP4 records
 constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
-// barriers: raw_full[4], raw_empty[4], kv_full[2], kv_free[2], s_full[2],
-// s_free[2], p_full[2], pv_done[2], q_full, final
-constexpr int kNumBars = 4 + 4 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort, raw valid[4]
+enum {
+  B_RAW_FULL = 0,
+  B_RAW_EMPTY = B_RAW_FULL + kRawStages,
+  B_K_FULL = B_RAW_EMPTY + kRawStages,
+  B_K_FREE = B_K_FULL + kKStages,
+  B_V_FULL = B_K_FREE + kKStages,
+  B_V_FREE = B_V_FULL + kVStages,
+  B_S_FULL = B_V_FREE + kVStages,
+  B_S_FREE = B_S_FULL + kSStages,
+  B_P_FULL = B_S_FREE + kSStages,
+  B_PV_DONE = B_P_FULL + kPStages,
+  B_Q_FULL = B_PV_DONE + kPStages,
+  B_FINAL = B_Q_FULL + 1,
+  kNumBars = B_FINAL + 1
+};
+constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort, raw valid[]
 constexpr int kSmemBytes = kMiscOff + 64 + 1024;
 static_assert(kSmemBytes <= 232448, "prefill shared memory plan too large");
 
-// TMEM columns: S double buffer at 0 and 32, O at 64 .. 319.
+// TMEM columns: the S ring at 0, 32, 64, 96; O at 128 .. 383.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 64;
+constexpr uint32_t kTmemO = kSStages * kBlockKeys;
+static_assert(kTmemO + 256 <= kTmemCols, "TMEM plan too large");
 
 struct PrefillArgs {
   int64_t num_pages;
@@ -202,33 +223,39 @@ __device__ bool find_tile(const PrefillArgs& a, int64_t idx, Tile* t) {
   return false;
 }
 
+// Parity of the phase in which item g of a ring of n slots lands in its slot.
+__device__ __forceinline__ uint32_t ring_parity(int64_t g, int n) { return static_cast<uint32_t>((g / n) & 1); }
+
 __device__ __forceinline__ uint64_t* bar_at(uint8_t* smem, int i) {
   return reinterpret_cast<uint64_t*>(smem + kBarOff) + i;
 }
-enum {
-  B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_KV_FULL = 8, B_KV_FREE = 10, B_S_FULL = 12, B_S_FREE = 14,
-  B_P_FULL = 16, B_PV_DONE = 18, B_Q_FULL = 20, B_FINAL = 21
-};
-
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile uint32_t* abort_flag = misc + 1;
-  uint32_t* raw_valid = misc + 2;  // [kRawStages] bit 0/1: page 0/1 loaded
+  uint32_t* raw_valid = misc + 2;  // [kRawStages] bit p: page p of the block loaded
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kRawStages; ++i) {
       mbar_init(bar_at(smem, B_RAW_FULL + i), 1);
-      mbar_init(bar_at(smem, B_RAW_EMPTY + i), 4);
+      mbar_init(bar_at(smem, B_RAW_EMPTY + i), kDequantWarps);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_at(smem, B_KV_FULL + i), 4);
-      mbar_init(bar_at(smem, B_KV_FREE + i), 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(bar_at(smem, B_K_FULL + i), kDequantWarps);
+      mbar_init(bar_at(smem, B_K_FREE + i), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(bar_at(smem, B_V_FULL + i), kDequantWarps);
+      mbar_init(bar_at(smem, B_V_FREE + i), 1);
+    }
+    for (int i = 0; i < kSStages; ++i) {
       mbar_init(bar_at(smem, B_S_FULL + i), 1);
       mbar_init(bar_at(smem, B_S_FREE + i), 4);
+    }
+    for (int i = 0; i < kPStages; ++i) {
       mbar_init(bar_at(smem, B_P_FULL + i), 4);
       mbar_init(bar_at(smem, B_PV_DONE + i), 1);
     }
@@ -284,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pages = (t.len + 15) >> 4;
       for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
         const int rs = static_cast<int>(gb % kRawStages);
-        if (lane == 0) ok = wait(B_RAW_EMPTY + rs, static_cast<uint32_t>((gb / kRawStages) & 1) ^ 1u);
+        if (lane == 0) ok = wait(B_RAW_EMPTY + rs, ring_parity(gb, kRawStages) ^ 1u);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         // lanes 0 and 1: the block's two pages
@@ -318,30 +345,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bounded drain of the loads that may still be landing
       const int64_t first = gb > kRawStages ? gb - kRawStages : 0;
       for (int64_t i = first; i < gb; ++i)
-        mbar_wait(bar_at(smem, B_RAW_FULL + static_cast<int>(i % kRawStages)),
-                  static_cast<uint32_t>((i / kRawStages) & 1));
+        mbar_wait(bar_at(smem, B_RAW_FULL + static_cast<int>(i % kRawStages)), ring_parity(i, kRawStages));
     }
-  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + 4) {
+  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
     // ----------------------------------------------------------- dequant
-    const int dt = threadIdx.x - kDequantWarp0 * 32;  // 0..127
+    const int dt = threadIdx.x - kDequantWarp0 * 32;  // 0 .. 32 * kDequantWarps - 1
+    constexpr int kDT = 32 * kDequantWarps;
     int64_t gb = 0;
     bool ok = true;
     Tile t;
     for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x) {
       for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
         const int rs = static_cast<int>(gb % kRawStages);
-        const int kb = static_cast<int>(gb & 1);
-        ok = wait_warp(B_RAW_FULL + rs, static_cast<uint32_t>((gb / kRawStages) & 1));
-        if (ok && gb >= 2) ok = wait_warp(B_KV_FREE + kb, static_cast<uint32_t>(((gb - 2) >> 1) & 1));
+        const int ks = static_cast<int>(gb % kKStages), vs = static_cast<int>(gb % kVStages);
+        ok = wait_warp(B_RAW_FULL + rs, ring_parity(gb, kRawStages));
+        // K slot: free once the QK of block gb - kKStages completed
+        if (ok && gb >= kKStages) ok = wait_warp(B_K_FREE + ks, ring_parity(gb - kKStages, kKStages));
         if (!ok) break;
         const uint32_t valid = raw_valid[rs];
         const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStageBytes);
-        uint8_t* ktile = smem + kKOff + kb * kKBytes;
-        uint8_t* vtile = smem + kVOff + kb * kVBytes;
-        // K: 512 units (key, 16-dim block), 4 per thread
+        uint8_t* ktile = smem + kKOff + ks * kKBytes;
+        uint8_t* vtile = smem + kVOff + vs * kVBytes;
+        // K: 512 units (key, 16-dim block)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = dt + 128 * i;
+        for (int i = 0; i < 512 / kDT; ++i) {
+          const int u = dt + kDT * i;
           const int key = u >> 4, blk = u & 15;
           const int pg = key >> 4, slot = key & 15;
           uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
@@ -361,38 +389,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk, 256)) = lo;
           *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk + 8, 256)) = hi;
         }
-        // V^T: 1,024 units (dim d, 8 keys), 8 per thread
-#pragma unroll 2
-        for (int i = 0; i < 8; ++i) {
-          const int u = dt + 128 * i;
-          const int d = u >> 2, c = u & 3;
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(smem, B_K_FULL + ks));
+        // V slot: free once the P V of block gb - kVStages completed
+        if (gb >= kVStages) ok = wait_warp(B_V_FREE + vs, ring_parity(gb - kVStages, kVStages));
+        if (!ok) break;
+        // V^T: 256 units (4 dims d0 .. d0+3, 8 keys 8c .. 8c+7): one 32-bit
+        // load of codes per slot pair (4 dims), widened pair by pair into the
+        // (key 2i, key 2i+1) registers of the four V^T rows
+#pragma unroll
+        for (int i = 0; i < 256 / kDT; ++i) {
+          const int u = dt + kDT * i;
+          const int d0 = 4 * (u >> 2), c = u & 3;
           const int pg = c >> 1;             // page of keys 8c .. 8c+7
           const int p0 = 4 * (c & 1);        // first slot pair in the page
-          uint4 out = make_uint4(0, 0, 0, 0);
+          uint32_t rows[4][4];               // [dim][slot pair] f16x2
           if ((valid >> pg) & 1) {
             const uint32_t rec = raw + pg * kRawPageBytes;
-            uint32_t o[4];
+            const int blk = d0 >> 4;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int pr = p0 + q;  // slot pair: slots 2pr, 2pr+1
-              const uint32_t code = lds8(rec + swz128(18 + 2 * pr + (d >> 7), d & 127));
+              const int pr = p0 + q;
+              const uint32_t codes = lds32(rec + swz128(18 + 2 * pr + (d0 >> 7), d0 & 127));
               const int s0 = 2 * pr, s1 = 2 * pr + 1;
-              const uint32_t sc0 = lds8(rec + swz128(34 + (s0 >> 3), (s0 & 7) * 16 + (d >> 4)));
-              const uint32_t sc1 = lds8(rec + swz128(34 + (s1 >> 3), (s1 & 7) * 16 + (d >> 4)));
-              uint32_t cv;
-              asm("{ .reg .b8 t; .reg .b16 w; cvt.u16.u32 w, %1; cvt.u8.u16 t, w; cvt.rn.f16x2.e2m1x2 %0, t; }"
-                  : "=r"(cv)
-                  : "r"(code));
-              o[q] = hmul2(cv, e4m3x2_to_f16x2(sc0 | (sc1 << 8)));
+              const uint32_t sc0 = lds8(rec + swz128(34 + (s0 >> 3), (s0 & 7) * 16 + blk));
+              const uint32_t sc1 = lds8(rec + swz128(34 + (s1 >> 3), (s1 & 7) * 16 + blk));
+              const uint32_t sp = e4m3x2_to_f16x2(sc0 | (sc1 << 8));
+              uint32_t cv[4];
+              e2m1x8_unpack(codes, cv);  // cv[x] = (slot 2pr, slot 2pr+1) of dim d0 + x
+#pragma unroll
+              for (int x = 0; x < 4; ++x) rows[x][q] = hmul2(cv[x], sp);
             }
-            out = make_uint4(o[0], o[1], o[2], o[3]);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) rows[x][q] = 0u;
           }
-          *reinterpret_cast<uint4*>(vtile + core_off(d, 8 * c, kBlockKeys)) = out;
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            *reinterpret_cast<uint4*>(vtile + core_off(d0 + x, 8 * c, kBlockKeys)) =
+                make_uint4(rows[x][0], rows[x][1], rows[x][2], rows[x][3]);
         }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar_at(smem, B_KV_FULL + kb));
+          mbar_arrive(bar_at(smem, B_V_FULL + vs));
           mbar_arrive(bar_at(smem, B_RAW_EMPTY + rs));
         }
       }
@@ -403,21 +446,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_base = smem_addr(smem + kQOff);
       const uint32_t idesc_qk = idesc_f16(128, kBlockKeys);
       const uint32_t idesc_pv = idesc_f16(128, 256);
-      int64_t gb = 0;     // next block whose QK is issued
+      int64_t gb = 0;  // first block of the current tile
       int64_t tcount = 0;
       bool ok = true, issued_any = false;
       Tile t;
       auto issue_qk = [&](int64_t g) -> bool {
-        const int kb = static_cast<int>(g & 1), sb = static_cast<int>(g & 1);
-        if (!wait(B_KV_FULL + kb, static_cast<uint32_t>((g >> 1) & 1))) return false;
-        if (g >= 2 && !wait(B_S_FREE + sb, static_cast<uint32_t>(((g - 2) >> 1) & 1))) return false;
+        const int ks = static_cast<int>(g % kKStages), ss = static_cast<int>(g % kSStages);
+        if (!wait(B_K_FULL + ks, ring_parity(g, kKStages))) return false;
+        if (g >= kSStages && !wait(B_S_FREE + ss, ring_parity(g - kSStages, kSStages))) return false;
         tc_fence_after();
-        const uint32_t k_base = smem_addr(smem + kKOff + kb * kKBytes);
+        const uint32_t k_base = smem_addr(smem + kKOff + ks * kKBytes);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
-          umma_f16(tmem + kTmemS + sb * kBlockKeys, smem_desc(q_base + kk * 256, 128, 4096),
+          umma_f16(tmem + kTmemS + ss * kBlockKeys, smem_desc(q_base + kk * 256, 128, 4096),
                    smem_desc(k_base + kk * 256, 128, 4096), idesc_qk, kk > 0);
-        umma_commit(bar_at(smem, B_S_FULL + sb));
+        umma_commit(bar_at(smem, B_S_FULL + ss));
+        umma_commit(bar_at(smem, B_K_FREE + ks));
         issued_any = true;
         return true;
       };
@@ -425,25 +469,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait(B_Q_FULL, static_cast<uint32_t>(tcount & 1));
         if (!ok) break;
         const int64_t g0 = gb;
-        ok = issue_qk(g0);
+        for (int j = 0; ok && j < min(kLookahead, t.nblocks); ++j) ok = issue_qk(g0 + j);
         for (int j = 0; ok && j < t.nblocks; ++j) {
           const int64_t g = g0 + j;
-          if (j + 1 < t.nblocks) {
-            ok = issue_qk(g + 1);
-            if (!ok) break;
-          }
-          const int pb = static_cast<int>(g & 1), kb = static_cast<int>(g & 1);
-          ok = wait(B_P_FULL + pb, static_cast<uint32_t>((g >> 1) & 1));
+          const int ps = static_cast<int>(g % kPStages), vs = static_cast<int>(g % kVStages);
+          ok = wait(B_P_FULL + ps, ring_parity(g, kPStages)) && wait(B_V_FULL + vs, ring_parity(g, kVStages));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t p_base = smem_addr(smem + kPOff + pb * kPBytes);
-          const uint32_t v_base = smem_addr(smem + kVOff + kb * kVBytes);
+          const uint32_t p_base = smem_addr(smem + kPOff + ps * kPBytes);
+          const uint32_t v_base = smem_addr(smem + kVOff + vs * kVBytes);
 #pragma unroll
           for (int kk = 0; kk < kBlockKeys / 16; ++kk)
             umma_f16(tmem + kTmemO, smem_desc(p_base + kk * 256, 128, 512), smem_desc(v_base + kk * 256, 128, 512),
                      idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar_at(smem, B_KV_FREE + kb));
-          umma_commit(bar_at(smem, B_PV_DONE + pb));
+          umma_commit(bar_at(smem, B_V_FREE + vs));
+          umma_commit(bar_at(smem, B_PV_DONE + ps));
+          if (j + kLookahead < t.nblocks) ok = issue_qk(g + kLookahead);
         }
         gb = g0 + t.nblocks;
       }
@@ -496,15 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t g0 = gb;
       for (int j = 0; j < t.nblocks; ++j) {
         const int64_t g = g0 + j;
-        const int sb = static_cast<int>(g & 1), pb = static_cast<int>(g & 1);
-        ok = wait_warp(B_S_FULL + sb, static_cast<uint32_t>((g >> 1) & 1));
+        const int ss = static_cast<int>(g % kSStages), ps = static_cast<int>(g % kPStages);
+        ok = wait_warp(B_S_FULL + ss, ring_parity(g, kSStages));
         if (!ok) break;
         tc_fence_after();
         uint32_t sr[32];
         {
           uint32_t x0[16], x1[16];
-          tmem_ld16(lane_addr + kTmemS + sb * kBlockKeys, x0);
-          tmem_ld16(lane_addr + kTmemS + sb * kBlockKeys + 16, x1);
+          tmem_ld16(lane_addr + kTmemS + ss * kBlockKeys, x0);
+          tmem_ld16(lane_addr + kTmemS + ss * kBlockKeys + 16, x1);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -514,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(smem, B_S_FREE + sb));
+        if (lane == 0) mbar_arrive(bar_at(smem, B_S_FREE + ss));
         float sv[32];
         float mb = -INFINITY;
         const int key0 = j * kBlockKeys;
@@ -527,13 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lazy rescale: move the exponent base only when the row max grows
         // by more than the threshold (or for the first finite max)
         float alpha = 1.f;
-        bool move = mb > m_used + kRescaleThreshold || (m_used == -INFINITY && mb > -INFINITY);
-        float base_new = move ? mb : m_used;
+        const bool move = mb > m_used + kRescaleThreshold || (m_used == -INFINITY && mb > -INFINITY);
+        const float base_new = move ? mb : m_used;
         if (move && m_used != -INFINITY) alpha = fast_exp2(m_used - base_new);
         // O holds this row's sum so far only after at least one P V
         const bool need = move && m_used != -INFINITY && j > 0;
         if (__any_sync(0xffffffffu, need)) {
-          ok = wait_warp(B_PV_DONE + static_cast<int>((g - 1) & 1), static_cast<uint32_t>(((g - 1) >> 1) & 1));
+          ok = wait_warp(B_PV_DONE + static_cast<int>((g - 1) % kPStages), ring_parity(g - 1, kPStages));
           if (!ok) break;
           tc_fence_after();
           const float f = need ? alpha : 1.f;
@@ -561,25 +602,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           add += f2.x + f2.y;
         }
         l += add;
-        // P buffer pb was last read by the P V of block g - 2
-        if (g >= 2) {
-          ok = wait_warp(B_PV_DONE + pb, static_cast<uint32_t>(((g - 2) >> 1) & 1));
+        // P slot ps was last read by the P V of block g - kPStages
+        if (g >= kPStages) {
+          ok = wait_warp(B_PV_DONE + ps, ring_parity(g - kPStages, kPStages));
           if (!ok) break;
         }
-        uint8_t* pt = smem + kPOff + pb * kPBytes;
+        uint8_t* pt = smem + kPOff + ps * kPBytes;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
               make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(smem, B_P_FULL + pb));
+        if (lane == 0) mbar_arrive(bar_at(smem, B_P_FULL + ps));
       }
       if (!ok) break;
       gb = g0 + t.nblocks;
       // epilogue: final O row, normalised, into the (sequence, KV head) slot
       const int64_t gl = gb - 1;
-      ok = wait_warp(B_PV_DONE + static_cast<int>(gl & 1), static_cast<uint32_t>((gl >> 1) & 1));
+      ok = wait_warp(B_PV_DONE + static_cast<int>(gl % kPStages), ring_parity(gl, kPStages));
       if (!ok) break;
       tc_fence_after();
       const int64_t seg = static_cast<int64_t>(t.b) * a.hkv + t.h;

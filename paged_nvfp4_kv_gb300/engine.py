@@ -24,7 +24,9 @@ def to_bf16(x, device):
 
 
 class DecodeSession:
-    def __init__(self, w, device="cuda", max_pos=None, stream=None):
+    def __init__(self, w, device="cuda", max_pos=None, stream=None, tables=None, inputs=None):
+        """``tables``: (cos, sin) of another session to share; ``inputs``: a
+        session whose new-token tensors (q, k, v) and index tensors to share."""
         self.w = w
         self.device = device
         self.stream = stream
@@ -37,9 +39,12 @@ class DecodeSession:
                                 y["beta_slow"], y["rotary_dim"], y.get("deployed", True))
         self.max_pos = int(max_pos or w.max_pos)
         half = self.rotary_dim // 2
-        self.cos = torch.empty(self.max_pos, half, dtype=torch.float32, device=device)
-        self.sin = torch.empty(self.max_pos, half, dtype=torch.float32, device=device)
-        yarn_rope_tables(self.yarn, self.max_pos, self.cos, self.sin, stream)
+        if tables is not None:
+            self.cos, self.sin = tables
+        else:
+            self.cos = torch.empty(self.max_pos, half, dtype=torch.float32, device=device)
+            self.sin = torch.empty(self.max_pos, half, dtype=torch.float32, device=device)
+            yarn_rope_tables(self.yarn, self.max_pos, self.cos, self.sin, stream)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
         self.max_qlen = int(w.qlen.max())
         self.group = w.num_q_heads // w.num_kv_heads
@@ -56,7 +61,9 @@ class DecodeSession:
         self.tok_pos = torch.from_numpy(pos).to(device)
         self.total_q = w.total_q
         # the step's new tokens (un-roped Q, K, V)
-        if self.total_q:
+        if inputs is not None:
+            self.q, self.k, self.v = inputs.q, inputs.k, inputs.v
+        elif self.total_q:
             self.q = to_bf16(np.concatenate([w.q_rows(b) for b in range(w.batch)]), device)
             self.k = to_bf16(np.concatenate([w.k_rows(b, int(w.cached[b]), int(w.seq_lens[b]))
                                              for b in range(w.batch)]), device)
@@ -108,3 +115,57 @@ class DecodeSession:
 
     def error_word(self):
         return int(self.dev_err.item())
+
+
+class DecodeStack:
+    """``layers`` attention layers of one geometry, each with its own pool,
+    stepped together; the step can be captured in a CUDA graph and replayed
+    (the library allocates nothing and every call is stream-ordered, so a
+    captured step is the same launches with the same arguments).
+
+    Layer 0 is filled from the workload; the other layers start as copies of
+    its pool (identical caches, distinct memory), and all layers append the
+    same new tokens."""
+
+    def __init__(self, w, layers=16, device="cuda"):
+        first = DecodeSession(w, device=device)
+        self.sessions = [first]
+        for _ in range(layers - 1):
+            self.sessions.append(DecodeSession(w, device=device, tables=(first.cos, first.sin),
+                                               inputs=first))
+        self.graph = None
+
+    def fill(self):
+        first = self.sessions[0]
+        first.fill()
+        for s in self.sessions[1:]:
+            s.cache.pool.copy_(first.cache.pool)
+
+    def step(self, out_fp32=False):
+        return [s.step(out_fp32) for s in self.sessions]
+
+    def capture(self, out_fp32=False):
+        """Capture one step of every layer in a CUDA graph (after one eager
+        step on the capture stream, which sets kernel attributes)."""
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            self.step(out_fp32)
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            self.step(out_fp32)
+        torch.cuda.current_stream().wait_stream(stream)
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
+
+    def outputs(self, out_fp32=False):
+        return [s.out32 if out_fp32 else s.out for s in self.sessions]
+
+    def error_word(self):
+        e = 0
+        for s in self.sessions:
+            e |= s.error_word()
+        return e

@@ -951,8 +951,12 @@ int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
 #define PNKV_NVFP4_NW 12
 #define PNKV_NVFP4_QS 0
 #endif
+#ifndef PNKV_NVFP4_NP
+#define PNKV_NVFP4_NP 1
+#endif
   if (rows <= 8)
-    return launch_decode<KVDT, 1, 1, fp4 ? PNKV_NVFP4_NW : 7, fp4 ? PNKV_NVFP4_QS : 0>(map, a, grid, stream);
+    return launch_decode<KVDT, 1, 1, fp4 ? PNKV_NVFP4_NW : 7, fp4 ? PNKV_NVFP4_QS : 0, fp4 ? PNKV_NVFP4_NP : 1>(
+        map, a, grid, stream);
   if (rows <= 16) return launch_decode<KVDT, 2, 1, 7>(map, a, grid, stream);
   if (rows <= 32) return launch_decode<KVDT, 2, 2, 7>(map, a, grid, stream);
   if (rows <= 64) return launch_decode<KVDT, 2, 4, 5>(map, a, grid, stream);

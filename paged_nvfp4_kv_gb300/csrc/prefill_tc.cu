@@ -13,19 +13,22 @@
 // A CTA tile is 128 TMEM lanes = 128 query rows of one KV head: T = 128 / G
 // consecutive query tokens times the G query heads that share the KV head
 // (GQA), so every KV byte read serves all G heads.  Keys are swept in
-// blocks of 32 (two 16-token pages):
-//   producer warp   TMA-loads the two pages' NVFP4 head records (raw ring)
-//   dequant warps   widen K to fp16 [32 keys][256 dims] and V to fp16
-//                   V^T [256 dims][32 keys] (E2M1 x E4M3 is exact in fp16),
+// blocks of 64 (four 16-token pages):
+//   producer warp   TMA-loads the four pages' NVFP4 head records (raw ring)
+//   dequant warps   widen K to fp16 [64 keys][256 dims] and V to fp16
+//                   V^T [256 dims][64 keys] (E2M1 x E4M3 is exact in fp16),
 //                   both in the no-swizzle K-major core-matrix layout
-//   MMA thread      S = Q K^T   (M 128, N 32, K 256)  -> TMEM, double buffer
-//                   O += P V    (M 128, N 256, K 32)  -> TMEM
+//   MMA thread      S = Q K^T   (M 128, N 64, K 256)  -> TMEM ring, with Q
+//                               (fp16) held in TMEM as the A operand, so
+//                               shared memory feeds only K
+//                   O += P V    (M 128, N 256, K 64)  -> TMEM
 //   softmax warps   one row per thread: tcgen05.ld of S, online softmax,
 //                   P (fp16) -> shared memory; O is rescaled in TMEM only when
 //                   a row's running maximum grows by more than 2^8, so the
 //                   exponentials stay below 256 and most blocks need no
-//                   rescale (the final normalisation divides by the sum of
-//                   the same fp16 values that entered P V)
+//                   rescale (the row sum adds the fp32 exponentials; P V
+//                   takes them rounded to fp16, a relative difference of at
+//                   most 2^-11 per term)
 // Per-tensor K/V scales fold into the logit scale and the output, as in the
 // decode path.  The CTA writes one normalised partial (with its natural-log
 // LSE) per row into the (sequence, KV head) slot, which split_kv_combine
@@ -40,39 +43,43 @@
 namespace pnkv {
 namespace {
 
-constexpr int kThreads = 448;         // 14 warps
+constexpr int kThreads = 480;         // 15 warps
 // warps 0-3 run the softmax, one TMEM lane quarter (32 rows) each
 constexpr int kDequantWarp0 = 4;      // warps 4-11
 constexpr int kDequantWarps = 8;
 constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kBlockKeys = 32;        // keys per KV block (two pages)
-// ring depths: QK runs up to kSStages - 1 blocks ahead of P V, so the softmax
-// of a block overlaps the tensor work of the next ones
-constexpr int kRawStages = 2;
-constexpr int kKStages = 4;
-constexpr int kVStages = 3;
-constexpr int kSStages = 4;
-constexpr int kPStages = 3;
-constexpr int kLookahead = kSStages - 1;
+constexpr int kMmaWarp = 13;          // issues P V; allocates TMEM
+constexpr int kQkWarp = 14;           // issues QK
+constexpr int kBlockKeys = 64;        // keys per KV block (four pages)
+constexpr int kBlockPages = kBlockKeys / 16;
+// ring depths.  The QK of block g waits for the softmax of block g - kSStages
+// to have loaded its S slot, so QK runs up to kSStages blocks ahead of the
+// softmax, and the softmax of a block overlaps the P V of the one before.
+constexpr int kRawStages = 3;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kSStages = 2;
+constexpr int kPStages = 2;
 constexpr int kRawPageBytes = 5120;   // 4,608-byte record, 1,024-aligned slot
-constexpr int kRawStageBytes = 2 * kRawPageBytes;
+constexpr int kRawStageBytes = kBlockPages * kRawPageBytes;
 constexpr uint32_t kRecBytes = 4608;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
-// Shared memory plan (offsets from a 1,024-byte aligned base).
-constexpr int kQOff = 0;                                  // 128 x 256 fp16
-constexpr int kQBytes = 128 * 256 * 2;
-constexpr int kKOff = kQOff + kQBytes;                    // ring of [32 x 256] fp16
+// Shared memory plan (offsets from a 1,024-byte aligned base).  Q lives in
+// TMEM (the A operand of S = Q K^T), so shared memory holds only the streamed
+// operands.
+constexpr int kKOff = 0;                                  // ring of [64 x 256] fp16
 constexpr int kKBytes = kBlockKeys * 256 * 2;
-constexpr int kVOff = kKOff + kKStages * kKBytes;         // ring of [256 x 32] fp16
+constexpr int kVOff = kKOff + kKStages * kKBytes;         // ring of [256 x 64] fp16
 constexpr int kVBytes = 256 * kBlockKeys * 2;
-constexpr int kPOff = kVOff + kVStages * kVBytes;         // ring of [128 x 32] fp16
+constexpr int kPOff = kVOff + kVStages * kVBytes;         // ring of [128 x 64] fp16
 constexpr int kPBytes = 128 * kBlockKeys * 2;
 constexpr int kRawOff = kPOff + kPStages * kPBytes;       // raw NVFP4 records
-constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
+constexpr int kScrOff = kRawOff + kRawStages * kRawStageBytes;  // per dequant warp: V scales
+constexpr int kScrWarpBytes = kBlockPages * 32;                 // [page][2 blocks][16 slots]
+constexpr int kBarOff = kScrOff + kDequantWarps * kScrWarpBytes;
 enum {
   B_RAW_FULL = 0,
   B_RAW_EMPTY = B_RAW_FULL + kRawStages,
@@ -92,11 +99,13 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort, r
 constexpr int kSmemBytes = kMiscOff + 64 + 1024;
 static_assert(kSmemBytes <= 232448, "prefill shared memory plan too large");
 
-// TMEM columns: the S ring at 0, 32, 64, 96; O at 128 .. 383.
+// TMEM columns: the S ring at 0 and 64; O at 128 .. 383; Q (fp16, two per
+// 32-bit column) at 384 .. 511.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = kSStages * kBlockKeys;
-static_assert(kTmemO + 256 <= kTmemCols, "TMEM plan too large");
+constexpr uint32_t kTmemQ = kTmemO + 256;
+static_assert(kTmemQ + 128 <= kTmemCols, "TMEM plan too large");
 
 struct PrefillArgs {
   int64_t num_pages;
@@ -148,6 +157,16 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       : "memory");
 }
 
+// Same with the A operand in TMEM (row i in lane i, two fp16 per column).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_addr(bar))
@@ -164,6 +183,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// 32 consecutive TMEM columns of this warp's 32 lanes into r[0 .. 31].
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -223,6 +253,13 @@ __device__ bool find_tile(const PrefillArgs& a, int64_t idx, Tile* t) {
   return false;
 }
 
+// Four E4M3 bytes as two fp16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // Parity of the phase in which item g of a ring of n slots lands in its slot.
 __device__ __forceinline__ uint32_t ring_parity(int64_t g, int n) { return static_cast<uint32_t>((g / n) & 1); }
 
@@ -260,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(smem, B_PV_DONE + i), 1);
     }
     mbar_init(bar_at(smem, B_Q_FULL), 4);
-    mbar_init(bar_at(smem, B_FINAL), 1);
+    mbar_init(bar_at(smem, B_FINAL), 2);  // one arrival per MMA-issuing thread
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -282,8 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
     *abort_flag = 1;
   };
-  // single-thread wait (the MMA issuer, producer lane 0)
+  // single-thread wait (the MMA issuer, producer lane 0); a completed phase
+  // returns at once, without reading the abort flag
   auto wait = [&](int bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar_at(smem, bar), parity)) return true;
     if (*abort_flag) return false;
     if (!mbar_wait(bar_at(smem, bar), parity)) {
       fail();
@@ -314,11 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ok = wait(B_RAW_EMPTY + rs, ring_parity(gb, kRawStages) ^ 1u);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        // lanes 0 and 1: the block's two pages
+        // lanes 0 .. kBlockPages - 1: the block's pages
         int32_t page = -1;
         bool in_seq = false;
-        if (lane < 2) {
-          const int pi = 2 * j + lane;
+        if (lane < kBlockPages) {
+          const int pi = kBlockPages * j + lane;
           in_seq = pi < pages;
           if (in_seq) {
             page = __ldg(row + pi);
@@ -328,13 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        const unsigned load = __ballot_sync(0xffffffffu, lane < 2 && page >= 0);
+        const unsigned load = __ballot_sync(0xffffffffu, lane < kBlockPages && page >= 0);
         if (lane == 0) {
           raw_valid[rs] = load;
           mbar_arrive_expect_tx(bar_at(smem, B_RAW_FULL + rs), __popc(load) * kRecBytes);
         }
         __syncwarp();
-        if (lane < 2 && page >= 0) {
+        if (lane < kBlockPages && page >= 0) {
           const int32_t y = (page * a.hkv + t.h) * 36;
           tma_load_2d(smem + kRawOff + rs * kRawStageBytes + lane * kRawPageBytes, &tmap, 0, y,
                       bar_at(smem, B_RAW_FULL + rs), policy);
@@ -366,28 +405,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStageBytes);
         uint8_t* ktile = smem + kKOff + ks * kKBytes;
         uint8_t* vtile = smem + kVOff + vs * kVBytes;
-        // K: 512 units (key, 16-dim block)
+        // K: 1,024 units (key, 16-dim block); the lanes of a warp take 32
+        // consecutive keys, so each quarter-warp stores one contiguous
+        // 128-byte core matrix (8 keys x 8 dims)
+        static_assert(kDequantWarps * 32 == 256, "unit mapping assumes 256 dequant threads");
+        // all loads first: a load may not pass an earlier shared-memory store
+        uint2 kw[4];
+        uint32_t ksb[4];
 #pragma unroll
-        for (int i = 0; i < 512 / kDT; ++i) {
-          const int u = dt + kDT * i;
-          const int key = u >> 4, blk = u & 15;
+        for (int i = 0; i < 4; ++i) {
+          const int key = (dt & 31) + 32 * (i & 1), blk = (dt >> 5) + 8 * (i >> 1);
           const int pg = key >> 4, slot = key & 15;
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          kw[i] = make_uint2(0, 0);
+          ksb[i] = 0;
           if ((valid >> pg) & 1) {
             const uint32_t rec = raw + pg * kRawPageBytes;
-            uint2 w;
-            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w.x), "=r"(w.y) : "r"(rec + swz128(slot, 8 * blk)));
-            const uint32_t sbyte = lds8(rec + swz128(16 + (slot >> 3), (slot & 7) * 16 + blk));
-            uint32_t s2 = e4m3x2_to_f16x2(sbyte);
-            s2 = prmt(s2, s2, 0x1010u);
-            uint32_t c0[4], c1[4];
-            e2m1x8_unpack(w.x, c0);
-            e2m1x8_unpack(w.y, c1);
-            lo = make_uint4(hmul2(c0[0], s2), hmul2(c0[1], s2), hmul2(c0[2], s2), hmul2(c0[3], s2));
-            hi = make_uint4(hmul2(c1[0], s2), hmul2(c1[1], s2), hmul2(c1[2], s2), hmul2(c1[3], s2));
+            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(kw[i].x), "=r"(kw[i].y) : "r"(rec + swz128(slot, 8 * blk)));
+            ksb[i] = lds8(rec + swz128(16 + (slot >> 3), (slot & 7) * 16 + blk));
           }
-          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk, 256)) = lo;
-          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk + 8, 256)) = hi;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int key = (dt & 31) + 32 * (i & 1), blk = (dt >> 5) + 8 * (i >> 1);
+          // a missing page has zero codes and a zero scale: fp16 zeros
+          uint32_t s2 = e4m3x2_to_f16x2(ksb[i]);
+          s2 = prmt(s2, s2, 0x1010u);
+          uint32_t c0[4], c1[4];
+          e2m1x8_unpack(kw[i].x, c0);
+          e2m1x8_unpack(kw[i].y, c1);
+          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk, 256)) =
+              make_uint4(hmul2(c0[0], s2), hmul2(c0[1], s2), hmul2(c0[2], s2), hmul2(c0[3], s2));
+          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk + 8, 256)) =
+              make_uint4(hmul2(c1[0], s2), hmul2(c1[1], s2), hmul2(c1[2], s2), hmul2(c1[3], s2));
         }
         fence_proxy_async();
         __syncwarp();
@@ -395,42 +444,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         // V slot: free once the P V of block gb - kVStages completed
         if (gb >= kVStages) ok = wait_warp(B_V_FREE + vs, ring_parity(gb - kVStages, kVStages));
         if (!ok) break;
-        // V^T: 256 units (4 dims d0 .. d0+3, 8 keys 8c .. 8c+7): one 32-bit
-        // load of codes per slot pair (4 dims), widened pair by pair into the
-        // (key 2i, key 2i+1) registers of the four V^T rows
+        // V^T: thread dt owns dim d = dt over the block's 64 keys.  The
+        // lanes of a warp read consecutive code bytes of a slot-pair row, and
+        // each quarter-warp stores one contiguous core matrix (8 dims x 8
+        // keys).  The block scales of the warp's two 16-dim blocks are first
+        // transposed through a per-warp scratch ([page][block][slot]), so a
+        // thread reads the 16 slot scales of its block with one 16-byte load.
+        {
+          const int d = dt;
+          const int wq = dt >> 5;
+          const uint32_t scr = smem_addr(smem + kScrOff + wq * kScrWarpBytes);
+          {
+            const int slot = lane & 15, bsel = lane >> 4, blk = 2 * wq + bsel;
 #pragma unroll
-        for (int i = 0; i < 256 / kDT; ++i) {
-          const int u = dt + kDT * i;
-          const int d0 = 4 * (u >> 2), c = u & 3;
-          const int pg = c >> 1;             // page of keys 8c .. 8c+7
-          const int p0 = 4 * (c & 1);        // first slot pair in the page
-          uint32_t rows[4][4];               // [dim][slot pair] f16x2
-          if ((valid >> pg) & 1) {
-            const uint32_t rec = raw + pg * kRawPageBytes;
-            const int blk = d0 >> 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int pr = p0 + q;
-              const uint32_t codes = lds32(rec + swz128(18 + 2 * pr + (d0 >> 7), d0 & 127));
-              const int s0 = 2 * pr, s1 = 2 * pr + 1;
-              const uint32_t sc0 = lds8(rec + swz128(34 + (s0 >> 3), (s0 & 7) * 16 + blk));
-              const uint32_t sc1 = lds8(rec + swz128(34 + (s1 >> 3), (s1 & 7) * 16 + blk));
-              const uint32_t sp = e4m3x2_to_f16x2(sc0 | (sc1 << 8));
-              uint32_t cv[4];
-              e2m1x8_unpack(codes, cv);  // cv[x] = (slot 2pr, slot 2pr+1) of dim d0 + x
-#pragma unroll
-              for (int x = 0; x < 4; ++x) rows[x][q] = hmul2(cv[x], sp);
+            for (int pg = 0; pg < kBlockPages; ++pg) {
+              const uint32_t b = ((valid >> pg) & 1)
+                                     ? lds8(raw + pg * kRawPageBytes + swz128(34 + (slot >> 3), (slot & 7) * 16 + blk))
+                                     : 0u;
+              asm volatile("st.shared.u8 [%0], %1;" ::"r"(scr + pg * 32 + bsel * 16 + slot), "h"(static_cast<uint16_t>(b)));
             }
-          } else {
+          }
+          __syncwarp();
+          const uint32_t code_row = 18 + (d >> 7), code_col = d & 127;
+          // all loads first (codes of the four pages, then their scales)
+          uint32_t code[kBlockPages][8];
+          uint4 sc[kBlockPages];
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
+          for (int pg = 0; pg < kBlockPages; ++pg) {
+            const uint32_t rec = raw + pg * kRawPageBytes;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) rows[x][q] = 0u;
+            for (int pr = 0; pr < 8; ++pr) code[pg][pr] = lds8(rec + swz128(code_row + 2 * pr, code_col));
+            sc[pg] = lds128(scr + pg * 32 + ((d >> 4) & 1) * 16);
           }
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
-            *reinterpret_cast<uint4*>(vtile + core_off(d0 + x, 8 * c, kBlockKeys)) =
-                make_uint4(rows[x][0], rows[x][1], rows[x][2], rows[x][3]);
+          for (int pg = 0; pg < kBlockPages; ++pg) {
+            // a missing page: its scales in the scratch are zero
+            uint32_t sf[8];  // fp16x2 scales of slot pairs 0 .. 7
+            e4m3x4_to_f16x2x2(sc[pg].x, sf[0], sf[1]);
+            e4m3x4_to_f16x2x2(sc[pg].y, sf[2], sf[3]);
+            e4m3x4_to_f16x2x2(sc[pg].z, sf[4], sf[5]);
+            e4m3x4_to_f16x2x2(sc[pg].w, sf[6], sf[7]);
+            uint32_t o[8];
+#pragma unroll
+            for (int pr = 0; pr < 8; ++pr) o[pr] = hmul2(e2m1x2_to_f16x2(code[pg][pr]), sf[pr]);
+            *reinterpret_cast<uint4*>(vtile + core_off(d, 16 * pg, kBlockKeys)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(vtile + core_off(d, 16 * pg + 8, kBlockKeys)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
         }
         fence_proxy_async();
         __syncwarp();
@@ -440,59 +499,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kQkWarp) {
     // --------------------------------------------------------------- MMA
+    // Two issuing threads in different warps: a shared-memory access of a
+    // thread (an mbarrier wait included) waits until the tensor core has
+    // taken the MMAs that thread issued before it, so the QK thread's waits
+    // never stall the P V stream and the other way round.
     if (lane == 0) {
-      const uint32_t q_base = smem_addr(smem + kQOff);
-      const uint32_t idesc_qk = idesc_f16(128, kBlockKeys);
-      const uint32_t idesc_pv = idesc_f16(128, 256);
+      const bool qk_role = warp == kQkWarp;
+      const uint32_t idesc = qk_role ? idesc_f16(128, kBlockKeys) : idesc_f16(128, 256);
       int64_t gb = 0;  // first block of the current tile
       int64_t tcount = 0;
       bool ok = true, issued_any = false;
       Tile t;
-      auto issue_qk = [&](int64_t g) -> bool {
-        const int ks = static_cast<int>(g % kKStages), ss = static_cast<int>(g % kSStages);
-        if (!wait(B_K_FULL + ks, ring_parity(g, kKStages))) return false;
-        if (g >= kSStages && !wait(B_S_FREE + ss, ring_parity(g - kSStages, kSStages))) return false;
-        tc_fence_after();
-        const uint32_t k_base = smem_addr(smem + kKOff + ks * kKBytes);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          umma_f16(tmem + kTmemS + ss * kBlockKeys, smem_desc(q_base + kk * 256, 128, 4096),
-                   smem_desc(k_base + kk * 256, 128, 4096), idesc_qk, kk > 0);
-        umma_commit(bar_at(smem, B_S_FULL + ss));
-        umma_commit(bar_at(smem, B_K_FREE + ks));
-        issued_any = true;
-        return true;
-      };
       for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x, ++tcount) {
-        ok = wait(B_Q_FULL, static_cast<uint32_t>(tcount & 1));
-        if (!ok) break;
         const int64_t g0 = gb;
-        for (int j = 0; ok && j < min(kLookahead, t.nblocks); ++j) ok = issue_qk(g0 + j);
-        for (int j = 0; ok && j < t.nblocks; ++j) {
-          const int64_t g = g0 + j;
-          const int ps = static_cast<int>(g % kPStages), vs = static_cast<int>(g % kVStages);
-          ok = wait(B_P_FULL + ps, ring_parity(g, kPStages)) && wait(B_V_FULL + vs, ring_parity(g, kVStages));
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t p_base = smem_addr(smem + kPOff + ps * kPBytes);
-          const uint32_t v_base = smem_addr(smem + kVOff + vs * kVBytes);
+        if (qk_role) {
+          // Q of this tile is in TMEM (written by the softmax warps)
+          ok = wait(B_Q_FULL, static_cast<uint32_t>(tcount & 1));
+          for (int j = 0; ok && j < t.nblocks; ++j) {
+            const int64_t g = g0 + j;
+            const int ks = static_cast<int>(g % kKStages), ss = static_cast<int>(g % kSStages);
+            ok = wait(B_K_FULL + ks, ring_parity(g, kKStages)) &&
+                 (g < kSStages || wait(B_S_FREE + ss, ring_parity(g - kSStages, kSStages)));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t k_base = smem_addr(smem + kKOff + ks * kKBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-            umma_f16(tmem + kTmemO, smem_desc(p_base + kk * 256, 128, 512), smem_desc(v_base + kk * 256, 128, 512),
-                     idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar_at(smem, B_V_FREE + vs));
-          umma_commit(bar_at(smem, B_PV_DONE + ps));
-          if (j + kLookahead < t.nblocks) ok = issue_qk(g + kLookahead);
+            for (int kk = 0; kk < 16; ++kk)  // 16 dims = 8 TMEM columns of Q per k-step
+              umma_f16_ta(tmem + kTmemS + ss * kBlockKeys, tmem + kTmemQ + kk * 8,
+                          smem_desc(k_base + kk * 256, 128, 4096), idesc, kk > 0);
+            umma_commit(bar_at(smem, B_S_FULL + ss));
+            umma_commit(bar_at(smem, B_K_FREE + ks));
+            issued_any = true;
+          }
+        } else {
+          for (int j = 0; ok && j < t.nblocks; ++j) {
+            const int64_t g = g0 + j;
+            const int ps = static_cast<int>(g % kPStages), vs = static_cast<int>(g % kVStages);
+            ok = wait(B_P_FULL + ps, ring_parity(g, kPStages)) && wait(B_V_FULL + vs, ring_parity(g, kVStages));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_base = smem_addr(smem + kPOff + ps * kPBytes);
+            const uint32_t v_base = smem_addr(smem + kVOff + vs * kVBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+              umma_f16(tmem + kTmemO, smem_desc(p_base + kk * 256, 128, kBlockKeys * 16),
+                       smem_desc(v_base + kk * 256, 128, kBlockKeys * 16), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(bar_at(smem, B_V_FREE + vs));
+            umma_commit(bar_at(smem, B_PV_DONE + ps));
+            issued_any = true;
+          }
         }
         gb = g0 + t.nblocks;
       }
       // every issued MMA completes before TMEM is released
-      if (issued_any) {
+      if (issued_any)
         umma_commit(bar_at(smem, B_FINAL));
-        mbar_wait(bar_at(smem, B_FINAL), 0);
-      }
+      else
+        mbar_arrive(bar_at(smem, B_FINAL));
+      mbar_wait(bar_at(smem, B_FINAL), 0);
     }
     __syncwarp();
   } else {
@@ -508,28 +574,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = r % a.group;
       const bool row_live = r < a.tpt * a.group && r / a.group < t.ntok;
       const int lim = !row_live ? 0 : (a.causal ? t.len - t.qlen + tok + 1 : t.len);
-      // Q row -> fp16, core-matrix layout (the previous tile's MMAs are done:
-      // its epilogue waited for the last P V)
+      // Q row -> fp16 into this thread's TMEM lane (the previous tile's MMAs
+      // are done: its epilogue waited for the last P V)
       {
-        uint8_t* qt = smem + kQOff;
         const uint4* src = row_live ? reinterpret_cast<const uint4*>(
                                           a.q + (static_cast<int64_t>(t.q0 + tok) * a.hq + t.h * a.group + head) * 256)
                                     : nullptr;
-#pragma unroll 4
-        for (int c = 0; c < 32; ++c) {
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (row_live) {
-            const uint4 w = __ldg(src + c);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {  // 32 dims = 16 columns per store
+          uint32_t h[16];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row_live) w = __ldg(src + 4 * c + v);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              h[e] = f32x2_to_f16x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xFFFF0000u));
-            o = make_uint4(h[0], h[1], h[2], h[3]);
+              h[4 * v + e] = f32x2_to_f16x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xFFFF0000u));
           }
-          *reinterpret_cast<uint4*>(qt + core_off(r, 8 * c, 256)) = o;
+          tmem_st16(lane_addr + kTmemQ + 16 * c, h);
         }
-        fence_proxy_async();
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_at(smem, B_Q_FULL));
       }
@@ -541,30 +607,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_warp(B_S_FULL + ss, ring_parity(g, kSStages));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[32];
-        {
-          uint32_t x0[16], x1[16];
-          tmem_ld16(lane_addr + kTmemS + ss * kBlockKeys, x0);
-          tmem_ld16(lane_addr + kTmemS + ss * kBlockKeys + 16, x1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            sr[e] = x0[e];
-            sr[16 + e] = x1[e];
-          }
-        }
+        uint32_t sr[kBlockKeys];
+        tmem_ld32(lane_addr + kTmemS + ss * kBlockKeys, sr);
+        tmem_ld32(lane_addr + kTmemS + ss * kBlockKeys + 32, sr + 32);
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_at(smem, B_S_FREE + ss));
-        float sv[32];
-        float mb = -INFINITY;
+        // the row maximum of the raw logits over the visible keys (masked
+        // keys become -inf); the logit scale is positive, so the maximum of
+        // the scaled logits is the scaled maximum
         const int key0 = j * kBlockKeys;
+        float mraw = -INFINITY;
+        if (__all_sync(0xffffffffu, key0 + kBlockKeys <= lim)) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float z = __uint_as_float(sr[k]) * a.qk_scale_log2;
-          sv[k] = (key0 + k < lim) ? z : -INFINITY;
-          mb = fmaxf(mb, sv[k]);
+          for (int k = 0; k < kBlockKeys; ++k) mraw = fmaxf(mraw, __uint_as_float(sr[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < kBlockKeys; ++k) {
+            if (key0 + k >= lim) sr[k] = __float_as_uint(-INFINITY);
+            mraw = fmaxf(mraw, __uint_as_float(sr[k]));
+          }
         }
+        const float mb = mraw * a.qk_scale_log2;
         // lazy rescale: move the exponent base only when the row max grows
         // by more than the threshold (or for the first finite max)
         float alpha = 1.f;
@@ -592,16 +657,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l *= alpha;
         m_used = base_new;
-        const float bse = (m_used == -INFINITY) ? 0.f : m_used;
-        uint32_t ph[16];
-        float add = 0.f;
+        // p = 2^(s * scale - base) (at most 2^threshold), P V takes p in fp16
+        // and l sums p in fp32
+        const float nbse = (m_used == -INFINITY) ? 0.f : -m_used;
+        uint32_t ph[kBlockKeys / 2];
+        float add0 = 0.f, add1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          ph[k] = f32x2_to_f16x2(fast_exp2(sv[2 * k] - bse), fast_exp2(sv[2 * k + 1] - bse));
-          const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&ph[k]));
-          add += f2.x + f2.y;
+        for (int k = 0; k < kBlockKeys / 2; ++k) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * k]), a.qk_scale_log2, nbse));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * k + 1]), a.qk_scale_log2, nbse));
+          ph[k] = f32x2_to_f16x2(p0, p1);
+          add0 += p0;
+          add1 += p1;
         }
-        l += add;
+        l += add0 + add1;
         // P slot ps was last read by the P V of block g - kPStages
         if (g >= kPStages) {
           ok = wait_warp(B_PV_DONE + ps, ring_parity(g - kPStages, kPStages));
@@ -609,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* pt = smem + kPOff + ps * kPBytes;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < kBlockKeys / 8; ++c)
           *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
               make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
         fence_proxy_async();

@@ -476,11 +476,11 @@ __device__ __forceinline__ void softmax_pages(WarpState<NTW>& st, float (&s)[NP]
   const int gid = lane >> 2;
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt) {
+    // maxima of the raw logits (masked keys -inf); the logit scale is
+    // positive, so the scaled maximum is the maximum of the scaled logits
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int pg = 0; pg < NP; ++pg) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[pg][nt][e] *= scale;
       if (masked[pg]) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -496,21 +496,24 @@ __device__ __forceinline__ void softmax_pages(WarpState<NTW>& st, float (&s)[NP]
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
-    const float mn0 = fmaxf(st.m[nt][0], mx0), mn1 = fmaxf(st.m[nt][1], mx1);
+    const float mn0 = fmaxf(st.m[nt][0], mx0 * scale), mn1 = fmaxf(st.m[nt][1], mx1 * scale);
     const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
     const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
     const float al0 = fast_exp2(st.m[nt][0] - base0), al1 = fast_exp2(st.m[nt][1] - base1);
     st.m[nt][0] = mn0;
     st.m[nt][1] = mn1;
+    // p = 2^(s * scale - base): P V takes p in fp16, l sums p in fp32
     float add0 = 0.f, add1 = 0.f;
 #pragma unroll
     for (int pg = 0; pg < NP; ++pg) {
-      const uint32_t x0 = f32x2_to_f16x2(fast_exp2(s[pg][nt][0] - base0), fast_exp2(s[pg][nt][1] - base1));
-      const uint32_t x1 = f32x2_to_f16x2(fast_exp2(s[pg][nt][2] - base0), fast_exp2(s[pg][nt][3] - base1));
-      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x0));
-      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x1));
-      add0 += f0.x + f1.x;
-      add1 += f0.y + f1.y;
+      const float p0 = fast_exp2(fmaf(s[pg][nt][0], scale, -base0));
+      const float p1 = fast_exp2(fmaf(s[pg][nt][1], scale, -base1));
+      const float p2 = fast_exp2(fmaf(s[pg][nt][2], scale, -base0));
+      const float p3 = fast_exp2(fmaf(s[pg][nt][3], scale, -base1));
+      const uint32_t x0 = f32x2_to_f16x2(p0, p1);
+      const uint32_t x1 = f32x2_to_f16x2(p2, p3);
+      add0 += p0 + p2;
+      add1 += p1 + p3;
       pb[pg][nt][0] = movmatrix_trans(x0);
       pb[pg][nt][1] = movmatrix_trans(x1);
     }
@@ -765,6 +768,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
     constexpr int64_t S = P::kStreams;
     const int64_t end = pc.i0 + pc.n;
     int64_t i = pc.i0 + ((stream - pc.i0 % S) % S + S) % S;
+    // stage and phase parity of unit i, advanced with 32-bit arithmetic
+    // (NP * S <= kStages, so one step wraps the ring at most once)
+    static_assert(NP * S <= P::kStages, "one iteration wraps the stage ring at most once");
+    int i_stage = static_cast<int>(i % P::kStages);
+    uint32_t i_par = static_cast<uint32_t>((i / P::kStages) & 1);
     for (; i < end; i += NP * S) {
       int64_t u[NP];
       bool here[NP];
@@ -774,9 +782,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int pg = 0; pg < NP; ++pg) {
         here[pg] = i + pg * S < end;
         u[pg] = here[pg] ? i + pg * S : i;
-        st_idx[pg] = static_cast<int>(u[pg] % P::kStages);
-        if (okw && here[pg])
-          okw = mbar_wait(&full[st_idx[pg]], static_cast<uint32_t>((u[pg] / P::kStages) & 1));
+        int idx = i_stage + (here[pg] ? pg * static_cast<int>(S) : 0);
+        uint32_t par = i_par;
+        if (idx >= P::kStages) {
+          idx -= P::kStages;
+          par ^= 1u;
+        }
+        st_idx[pg] = idx;
+        if (okw && here[pg]) okw = mbar_wait(&full[idx], par);
+      }
+      i_stage += NP * static_cast<int>(S);
+      if (i_stage >= P::kStages) {
+        i_stage -= P::kStages;
+        i_par ^= 1u;
       }
       if (!okw) {
         if (lane == 0) flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
@@ -951,15 +969,23 @@ int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
 #define PNKV_NVFP4_NW 12
 #define PNKV_NVFP4_QS 0
 #endif
+// two n-tiles (9 .. 64 rows per KV head): Q fragments staged in shared
+// memory or held in registers, pages per consumer iteration
+#ifndef PNKV_WIDE_QS
+#define PNKV_WIDE_QS 1
+#endif
+#ifndef PNKV_WIDE_NP
+#define PNKV_WIDE_NP 2
+#endif
 #ifndef PNKV_NVFP4_NP
 #define PNKV_NVFP4_NP 1
 #endif
   if (rows <= 8)
     return launch_decode<KVDT, 1, 1, fp4 ? PNKV_NVFP4_NW : 7, fp4 ? PNKV_NVFP4_QS : 0, fp4 ? PNKV_NVFP4_NP : 1>(
         map, a, grid, stream);
-  if (rows <= 16) return launch_decode<KVDT, 2, 1, 7>(map, a, grid, stream);
-  if (rows <= 32) return launch_decode<KVDT, 2, 2, 7>(map, a, grid, stream);
-  if (rows <= 64) return launch_decode<KVDT, 2, 4, 5>(map, a, grid, stream);
+  if (rows <= 16) return launch_decode<KVDT, 2, 1, 7, PNKV_WIDE_QS, PNKV_WIDE_NP>(map, a, grid, stream);
+  if (rows <= 32) return launch_decode<KVDT, 2, 2, 7, PNKV_WIDE_QS, PNKV_WIDE_NP>(map, a, grid, stream);
+  if (rows <= 64) return launch_decode<KVDT, 2, 4, 5, PNKV_WIDE_QS, PNKV_WIDE_NP>(map, a, grid, stream);
   return PNKV_ERR_UNSUPPORTED;
 }
 

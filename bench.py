@@ -40,7 +40,8 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", type=int, default=3, help="workload number (1..4)")
+    p.add_argument("--config", type=int, default=3,
+                   help="workload number: 1..5 as in the workload table, 6 = reduced chunked prefill (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     return p.parse_args()
@@ -356,7 +357,8 @@ def run_ours(args):
                 "frac": achieved / peak, "traffic": profiled_traffic(w.kv_dtype),
                 "peak_kind": peak_kind, "kernel": "paged_decode_attention",
                 "algorithmic_bytes_per_launch": algo_bytes}
-    if int(w.total_q) * w.num_q_heads // w.num_kv_heads > 64 * w.batch:
+    tile_path = int(w.qlen.max()) * (w.num_q_heads // w.num_kv_heads) > 64
+    if tile_path:
         # the tensor-core tile path: a dense contraction, judged against the
         # tensor peak (QK^T and PV, 2 FLOP per multiply-add, causal-exact)
         flops = attention_flops(w)
@@ -380,7 +382,8 @@ def run_ours(args):
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * K,
+        # per step: append, decode (plus its metadata kernel on the tile path), combine
+        "gpu_launches": (4 if tile_path else 3) * K,
         "clocks": clocks.summary(),
         "dev_err": err,
     }

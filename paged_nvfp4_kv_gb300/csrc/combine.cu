@@ -30,19 +30,38 @@ struct CombineArgs {
   float* lse_out;
 };
 
-// One 64-thread block per output row; thread j owns dims 4j .. 4j+3.  The
-// split weights are formed once in shared memory, then every thread streams
-// its float4 of each split (independent loads, so many are in flight).
-constexpr int kThreads = 64;
-constexpr int kMaxCached = 1024;  // splits whose weights fit in shared memory
+// One 256-thread block per output row.  The row's split LSEs are read once
+// into shared memory (max, then weights); then four groups of 64 threads each
+// stream every fourth split (thread j of a group owns dims 4j .. 4j+3), so
+// four times as many loads are in flight, and the groups' sums are added in a
+// fixed order.
+constexpr int kThreads = 256;
+constexpr int kGroups = kThreads / 64;
+constexpr int kMaxCached = 1024;  // splits whose LSE and weight fit in shared memory
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, x) : v + x;
+  }
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int i = 1; i < kThreads / 32; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+  __syncthreads();
+  return r;
+}
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
   __shared__ float w_s[kMaxCached];
   __shared__ float red[kThreads / 32];
-  __shared__ float bcast[2];
+  __shared__ float4 part[kGroups - 1][64];
   griddep_wait();
   griddep_launch_dependents();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   const int64_t t = row / a.hq;
   const int h = static_cast<int>(row - t * a.hq);
@@ -60,41 +79,38 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
   const int r = static_cast<int>((t - __ldg(a.qo_indptr + b)) * a.group + h % a.group);
   if (!(cnt > 0 && first >= 0 && r < a.rows_per_slot)) cnt = 0;
   const float* lse = a.lse_part + static_cast<int64_t>(first) * a.rows_per_slot + r;
+  auto lse_at = [&](int s) -> float {
+    return s < kMaxCached ? w_s[s] : __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot);
+  };
 
-  // M = max_s lse_s
+  // M = max_s lse_s (the LSEs are kept in w_s)
   float M = -INFINITY;
-  for (int s = tid; s < cnt; s += kThreads) M = fmaxf(M, __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = fmaxf(red[0], red[1]);
-  __syncthreads();
-  // weights e^(lse_s - M) and their sum
+  for (int s = tid; s < cnt; s += kThreads) {
+    const float l = __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot);
+    if (s < kMaxCached) w_s[s] = l;
+    M = fmaxf(M, l);
+  }
+  M = block_reduce(M, true, red);
+  // weights e^(lse_s - M) in place, and their sum
   float wsum = 0.f;
   if (M != -INFINITY) {
     for (int s = tid; s < cnt; s += kThreads) {
-      const float l = __ldg(lse + static_cast<int64_t>(s) * a.rows_per_slot);
+      const float l = lse_at(s);
       const float w = (l == -INFINITY) ? 0.f : expf(l - M);
       if (s < kMaxCached) w_s[s] = w;
       wsum += w;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  if (lane == 0) red[warp] = wsum;
-  __syncthreads();
-  if (tid == 0) bcast[0] = red[0] + red[1];
-  __syncthreads();
-  wsum = bcast[0];
+  wsum = block_reduce(wsum, false, red);  // (its barrier also publishes w_s)
 
+  const int g = tid >> 6, j = tid & 63;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (wsum > 0.f) {
     const float4* src = reinterpret_cast<const float4*>(
-        a.o_part + (static_cast<int64_t>(first) * a.rows_per_slot + r) * 256) + tid;
+        a.o_part + (static_cast<int64_t>(first) * a.rows_per_slot + r) * 256) + j;
     const int64_t step = static_cast<int64_t>(a.rows_per_slot) * 64;  // float4s per slot
 #pragma unroll 4
-    for (int s = 0; s < cnt; ++s) {
+    for (int s = g; s < cnt; s += kGroups) {
       float w;
       if (s < kMaxCached) {
         w = w_s[s];
@@ -108,21 +124,35 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
       acc.z += w * x.z;
       acc.w += w * x.w;
     }
-    const float inv = 1.f / wsum;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
   }
-  const int64_t base = row * 256 + 4 * tid;
-  if (a.out_fp32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + base) = acc;
-  } else {
-    const uint32_t w0 = f32_to_bf16_bits(acc.x) | (f32_to_bf16_bits(acc.y) << 16);
-    const uint32_t w1 = f32_to_bf16_bits(acc.z) | (f32_to_bf16_bits(acc.w) << 16);
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + base) = make_uint2(w0, w1);
+  if (g > 0) part[g - 1][j] = acc;
+  __syncthreads();
+  if (g == 0) {
+#pragma unroll
+    for (int k = 0; k < kGroups - 1; ++k) {
+      const float4 x = part[k][j];
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    if (wsum > 0.f) {
+      const float inv = 1.f / wsum;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+    }
+    const int64_t base = row * 256 + 4 * j;
+    if (a.out_fp32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + base) = acc;
+    } else {
+      const uint32_t w0 = f32_to_bf16_bits(acc.x) | (f32_to_bf16_bits(acc.y) << 16);
+      const uint32_t w1 = f32_to_bf16_bits(acc.z) | (f32_to_bf16_bits(acc.w) << 16);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + base) = make_uint2(w0, w1);
+    }
+    if (a.lse_out && j == 0) a.lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
   }
-  if (a.lse_out && tid == 0) a.lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
 }  // namespace

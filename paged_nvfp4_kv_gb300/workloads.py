@@ -212,5 +212,12 @@ def chunked_prefill(seed=1005):
                  [1040384], [8192])
 
 
+def chunked_prefill_reduced(seed=1005):
+    """The chunked-prefill shape at a size an ncu capture finishes in seconds:
+    200,000 cached NVFP4 tokens plus a 1,024-token chunk (profiling only)."""
+    return build("chunked prefill, reduced (1,024 queries over 201,024 NVFP4 keys)", seed, "nvfp4",
+                 [200000], [1024])
+
+
 CONFIGS = {1: tiny_decode, 2: native_window_decode, 3: million_token_decode,
-           4: multi_session_verify, 5: chunked_prefill}
+           4: multi_session_verify, 5: chunked_prefill, 6: chunked_prefill_reduced}

@@ -183,7 +183,7 @@ def oracle_rate(w, seconds, max_keys=None):
     from oracle import yarn as OY
 
     L = int(w.seq_lens[0])
-    dtype = OP.NVFP4 if w.kv_dtype == "nvfp4" else OP.BF16
+    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "bf16": OP.BF16}[w.kv_dtype]
     R = w.yarn["rotary_dim"]
 
     def run(n):

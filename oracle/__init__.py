@@ -18,6 +18,9 @@ Sources, cited by page title and section:
 * "262,144 Tokens on One RTX 5090: Qwen3.8-27B with an NVFP4 KV Cache That
   Actually Works" (stondo.github.io), sections "Why NVFP4 KV changes the math"
   and "The stack, for the impatient".
+* "A 1,048,576-token context on two RTX 5090s", section "Against vLLM:
+  prefill loses, decode wins, and one surprise" (the comparison engine's fp8
+  KV cache).
 * The published YaRN method (Peng et al., 2023, "YaRN: Efficient Context
   Window Extension of Large Language Models"), which the first page cites as
   its reference 3, for the NTK-by-parts ramp and the attention temperature.
@@ -28,6 +31,7 @@ Modules:
   formats    E2M1 / E4M3 / bf16 codecs.
   yarn       YaRN inverse frequencies, mscale, cos/sin tables, rope.
   nvfp4      two-level NVFP4 block quantise / dequantise.
+  fp8        per-tensor FP8 (E4M3) quantise / dequantise.
   paged      page-pool byte layout, scatter and gather.
   attention  dense and paged attention, split-KV partials, LSE combine.
 

@@ -22,22 +22,31 @@ Inside a page the record of each KV head h is contiguous, heads in order:
   (V pairs slots rather than elements because the P.V product reduces over
   tokens: one byte then widens to the two consecutive-token values a
   tensor-core operand register holds.)
+  FP8 (8,192 bytes per page-head; E4M3 codes, one scale per tensor):
+    K codes   [16 slots][D bytes]     element d of slot s at byte d
+    V codes   [8 slot pairs][D][2]    bytes 2d, 2d+1 of pair i: element d
+                                      of slots 2i, 2i+1 (the same pairing as
+                                      NVFP4, one byte per element)
   bf16 (16,384 bytes per page-head):
     K [16 slots][D] bf16 (little-endian), then V [16 slots][D] bf16
 """
 import numpy as np
 
+from . import fp8
 from .formats import bf16_bits, bf16_from_bits
 from .nvfp4 import dequantize, pack_nibbles, quantize, unpack_nibbles
 
 PAGE = 16
 NVFP4 = "nvfp4"
+FP8 = "fp8"
 BF16 = "bf16"
 
 
 def page_head_bytes(dtype, head_dim):
     if dtype == NVFP4:
         return 2 * PAGE * (head_dim // 2 + head_dim // 16)
+    if dtype == FP8:
+        return 2 * PAGE * head_dim
     return 2 * PAGE * head_dim * 2
 
 
@@ -55,6 +64,8 @@ def _sections(dtype, head_dim):
         v0 = ks + PAGE * sb
         vs = v0 + PAGE * cb
         return (k0, cb), (ks, sb), (v0, head_dim), (vs, sb)
+    if dtype == FP8:
+        return (0, head_dim), None, (PAGE * head_dim, 2 * head_dim), None
     rb = head_dim * 2
     return (0, rb), None, (PAGE * rb, rb), None
 
@@ -76,6 +87,9 @@ def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, 
         kq, kscale = quantize(k, g_k)
         vq, vscale = quantize(v, g_v)
         krow = pack_nibbles(kq)
+    elif dtype == FP8:
+        krow = fp8.quantize(k, g_k)
+        vq = fp8.quantize(v, g_v)
     else:
         krow = bf16_bits(k).view(np.uint8).reshape(k.shape[0], num_kv_heads, -1)
         vrow = bf16_bits(v).view(np.uint8).reshape(v.shape[0], num_kv_heads, -1)
@@ -96,6 +110,10 @@ def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, 
                 (ko, ksb), (vo, vsb) = ks, vs
                 pool[page, base + ko + slot * ksb: base + ko + (slot + 1) * ksb] = kscale[t, h]
                 pool[page, base + vo + slot * vsb: base + vo + (slot + 1) * vsb] = vscale[t, h]
+            elif dtype == FP8:
+                # byte 2d + (slot odd) of the pair's row
+                row0 = base + v0 + (slot // 2) * vb + (slot % 2)
+                pool[page, row0: row0 + vb: 2] = vq[t, h]
             else:
                 pool[page, base + v0 + slot * vb: base + v0 + (slot + 1) * vb] = vrow[t, h]
     return pool
@@ -115,6 +133,9 @@ def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, sta
         kq, kscale = quantize(k, g_k)
         vq, vscale = quantize(v, g_v)
         krow = pack_nibbles(kq)
+    elif dtype == FP8:
+        krow = fp8.quantize(k, g_k)
+        vq = fp8.quantize(v, g_v)
     else:
         krow = bf16_bits(k).view(np.uint8).reshape(T, num_kv_heads, -1)
         vrow = bf16_bits(v).view(np.uint8).reshape(T, num_kv_heads, -1)
@@ -138,6 +159,9 @@ def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, sta
             for j in range(ksb):
                 pool[pages, base + ko + slots * ksb + j] = kscale[:, h, j]
                 pool[pages, base + vo + slots * vsb + j] = vscale[:, h, j]
+        elif dtype == FP8:
+            for d in range(head_dim):
+                pool[pages, base + v0 + (slots // 2) * vb + 2 * d + (slots % 2)] = vq[:, h, d]
         else:
             for j in range(vb):
                 pool[pages, base + v0 + slots * vb + j] = vrow[:, h, j]
@@ -167,6 +191,10 @@ def gather_sequence(pool, dtype, num_kv_heads, head_dim, pages_of_seq, seq_len, 
         kk = dequantize(unpack_nibbles(krow), pool[pages[:, None], kscol], g_k)
         vv = dequantize(vcodes, pool[pages[:, None], vscol], g_v)
         return kk, vv
+    if dtype == FP8:
+        vcols = (base + v0 + (slots[:, None] // 2) * vb + 2 * np.arange(head_dim)[None, :]
+                 + (slots % 2)[:, None])
+        return fp8.dequantize(krow, g_k), fp8.dequantize(pool[pages[:, None], vcols], g_v)
     vcols = base + v0 + slots[:, None] * vb + np.arange(vb)[None, :]
     vrow = pool[pages[:, None], vcols]
     kk = bf16_from_bits(krow.view(np.uint16))

@@ -426,7 +426,13 @@ __device__ __forceinline__ void qk_nvfp4(uint32_t sb, int lane, const Q& qf, flo
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] = (acc[0][nt][e] + acc[1][nt][e]) + (acc[2][nt][e] + acc[3][nt][e]);
+    for (int e = 0; e < 4; ++e) {
+      // only the NA sets in use (adding a zero set is not free: x + 0 is not x for x = -0)
+      float v = acc[0][nt][e];
+#pragma unroll
+      for (int j = 1; j < NA; ++j) v += acc[j][nt][e];
+      s[nt][e] = v;
+    }
 }
 
 // S^T for one page: bf16 cache (four independent accumulator sets, as above).

@@ -51,7 +51,7 @@ class Workload:
     positions that the step appends and attends with."""
     name: str
     seed: int
-    kv_dtype: str                     # "nvfp4" or "bf16"
+    kv_dtype: str                     # "nvfp4", "fp8" or "bf16"
     cached: np.ndarray                # [B] int64
     qlen: np.ndarray                  # [B] int64
     num_q_heads: int = HQ
@@ -88,17 +88,22 @@ class Workload:
         return int(self.seq_lens.max())
 
     @property
+    def _code_top(self):
+        """Largest encodable magnitude per unit of g: E2M1 x E4M3 for NVFP4,
+        E4M3 for FP8."""
+        return E2M1_TOP * E4M3_TOP if self.kv_dtype == "nvfp4" else E4M3_TOP
+
+    @property
     def g_k(self):
         """Per-tensor K decode scale: a 6-sigma value of the widest channel,
         after the rope's mscale and the sqrt(2) a rotation can add, maps to
-        the top of the E2M1 x E4M3 range."""
+        the top of the code range."""
         m = 0.1 * math.log(self.yarn["factor"]) + 1.0 if self.yarn["factor"] > 1 else 1.0
-        return float(np.float32(6.0 * float(self.c_k.max()) * m * math.sqrt(2.0)
-                                / (E2M1_TOP * E4M3_TOP)))
+        return float(np.float32(6.0 * float(self.c_k.max()) * m * math.sqrt(2.0) / self._code_top))
 
     @property
     def g_v(self):
-        return float(np.float32(6.0 * float(self.c_v.max()) / (E2M1_TOP * E4M3_TOP)))
+        return float(np.float32(6.0 * float(self.c_v.max()) / self._code_top))
 
     # ---- values ----------------------------------------------------------
     def _rng(self, tensor, b, chunk):
@@ -219,5 +224,11 @@ def chunked_prefill_reduced(seed=1005):
                  [200000], [1024])
 
 
+def million_token_decode_fp8(seed=1003):
+    """The million-token decode with an FP8 (E4M3, per-tensor scale) cache."""
+    return build("million-token decode (1,048,576 FP8 keys)", seed, "fp8", [1048575], [1])
+
+
 CONFIGS = {1: tiny_decode, 2: native_window_decode, 3: million_token_decode,
-           4: multi_session_verify, 5: chunked_prefill, 6: chunked_prefill_reduced}
+           4: multi_session_verify, 5: chunked_prefill, 6: chunked_prefill_reduced,
+           7: million_token_decode_fp8}

@@ -150,7 +150,7 @@ def test_bf16_page_layout_offsets_by_hand():
     assert np.count_nonzero(pool) == 3
 
 
-@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.BF16])
+@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.FP8, PG.BF16])
 def test_scatter_gather_roundtrip_and_fast_path(dtype):
     rng = np.random.default_rng(27)
     L, H = 70, 4
@@ -158,11 +158,13 @@ def test_scatter_gather_roundtrip_and_fast_path(dtype):
     table = rng.permutation(8).astype(np.int32)[None, :5]
     p1 = PG.new_pool(8, dtype, H, D)
     p2 = PG.new_pool(8, dtype, H, D)
-    PG.scatter_tokens(p1, dtype, H, D, table, np.zeros(L, int), np.arange(L), k, v, 0.004, 0.003)
-    PG.scatter_sequence_fast(p2, dtype, H, D, table[0], 0, k, v, 0.004, 0.003)
+    # per-tensor scales that put the data's range at the top of the codes
+    gk, gv = (0.004, 0.003) if dtype != PG.FP8 else (0.024, 0.018)
+    PG.scatter_tokens(p1, dtype, H, D, table, np.zeros(L, int), np.arange(L), k, v, gk, gv)
+    PG.scatter_sequence_fast(p2, dtype, H, D, table[0], 0, k, v, gk, gv)
     assert np.array_equal(p1, p2)
     for h in range(H):
-        kk, vv = PG.gather_sequence(p1, dtype, H, D, table[0], L, h, 0.004, 0.003)
+        kk, vv = PG.gather_sequence(p1, dtype, H, D, table[0], L, h, gk, gv)
         if dtype == PG.BF16:
             assert np.array_equal(kk, k[:, h]) and np.array_equal(vv, v[:, h])
         else:
@@ -170,12 +172,12 @@ def test_scatter_gather_roundtrip_and_fast_path(dtype):
             assert np.corrcoef(kk.ravel(), k[:, h].ravel())[0, 1] > 0.98
 
 
-@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.BF16])
+@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.FP8, PG.BF16])
 def test_paged_decode_matches_dense_and_is_permutation_invariant(dtype):
     rng = np.random.default_rng(28)
     H, G, lens, qlen = 2, 3, [40, 23], [1, 5]
     Hq = H * G
-    g_k, g_v = 0.003, 0.002
+    g_k, g_v = (0.003, 0.002) if dtype != PG.FP8 else (0.018, 0.012)
     tot = sum(lens)
     npg = [(n + 15) // 16 for n in lens]
     perm = rng.permutation(sum(npg)).astype(np.int32)

@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "1M-ctx paged decode attention: KV tokens/s/layer and HBM GB/s (% of GB300 peak)"
 UNIT = "KV tokens/s/layer"
 FALLBACK_HBM_GBS = 6800.0   # earlier GB300 copy measurement, used if no measured peaks file
-ALGO_BYTES_PER_TOKEN = {"nvfp4": 4 * 2 * (128 + 16), "bf16": 4 * 2 * 256 * 2}
+ALGO_BYTES_PER_TOKEN = {"nvfp4": 4 * 2 * (128 + 16), "fp8": 4 * 2 * 256, "bf16": 4 * 2 * 256 * 2}
 
 
 def parse():

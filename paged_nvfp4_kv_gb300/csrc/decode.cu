@@ -69,8 +69,8 @@ struct DecodeArgs {
   int64_t num_pages;
   int32_t hkv;
   int32_t group;          // query heads per KV head
-  float qk_scale_log2;    // sm_scale * log2(e) (* k_scale for NVFP4)
-  float out_scale;        // v_scale for NVFP4, 1 for bf16
+  float qk_scale_log2;    // sm_scale * log2(e) (* k_scale for NVFP4 and FP8)
+  float out_scale;        // v_scale for NVFP4 and FP8, 1 for bf16
   const uint16_t* q;      // roped bf16 queries [total_q, hq, 256]
   const int32_t* qo_indptr;
   const int32_t* page_table;
@@ -95,6 +95,12 @@ struct Geometry<PNKV_KV_NVFP4> {
   static constexpr int kBoxRows = 36;      // 4,608 B head record
   static constexpr int kStageBytes = 5120; // next multiple of 1,024
   static constexpr uint32_t kTxBytes = 4608;
+};
+template <>
+struct Geometry<PNKV_KV_FP8> {
+  static constexpr int kBoxRows = 64;      // 8,192 B head record
+  static constexpr int kStageBytes = 8192;
+  static constexpr uint32_t kTxBytes = 8192;
 };
 template <>
 struct Geometry<PNKV_KV_BF16> {
@@ -347,7 +353,7 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, const Piece& pc, int
         for (int e = 0; e < 4; ++e) {
           const int word = 4 * c + e;  // dims 64*tig + 2*word, +1
           uint32_t v = ws[e];
-          if (KVDT == PNKV_KV_NVFP4)
+          if (KVDT != PNKV_KV_BF16)
             v = f32x2_to_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
           qb[nt][word >> 1][word & 1] = v;
         }
@@ -579,6 +585,99 @@ __device__ __forceinline__ void pv_nvfp4(uint32_t sb, int lane, WarpState<NTW>& 
       af[1] = hmul2(c1[bi], s_a_hi);  // dim 128 + 16*gid + mt
       af[2] = hmul2(c2[bi], s_b_lo);  // tokens 2tig+8, 2tig+9
       af[3] = hmul2(c3[bi], s_b_hi);
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// S^T for one page: FP8 cache.  Token t's codes are box rows 2t, 2t+1; for
+// k-step kk lane (gid, tig) takes dims 64*tig + 4*kk .. +3 of tokens gid and
+// gid+8 (the NVFP4 path's k order, so the same Q fragments serve), i.e. bytes
+// 64*(tig & 1) + 4*kk of box row 2*token + tig/2: four 16-byte loads per
+// token.  E4M3 widens exactly to fp16; the per-tensor scale folds into the
+// logit scale.
+template <int NTW, typename Q>
+__device__ __forceinline__ void qk_fp8(uint32_t sb, int lane, const Q& qf, float (&s)[NTW][4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  constexpr int NA = PNKV_QK_ACC;
+  float acc[4][NTW][4];
+#pragma unroll
+  for (int j = 0; j < NA; ++j)
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+  const int rlo = 2 * gid + (tig >> 1), rhi = 2 * (gid + 8) + (tig >> 1);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // 16-byte chunk 4*(tig & 1) + c: k-steps 4c .. 4c+3
+    const uint4 klo = lds128(sb + swz128(rlo, 16 * (4 * (tig & 1) + c)));
+    const uint4 khi = lds128(sb + swz128(rhi, 16 * (4 * (tig & 1) + c)));
+    const uint32_t wl[4] = {klo.x, klo.y, klo.z, klo.w};
+    const uint32_t wh[4] = {khi.x, khi.y, khi.z, khi.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int kk = 4 * c + q;
+      uint32_t af[4];
+      e4m3x4_to_f16x2x2(wl[q], af[0], af[2]);  // token gid: dims +0,+1 and +2,+3
+      e4m3x4_to_f16x2x2(wh[q], af[1], af[3]);  // token gid+8
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) {
+        const uint2 qv = qf.get(nt, kk);
+        mma_f16_16816(acc[kk % NA][nt], af, qv.x, qv.y);
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = acc[0][nt][e];
+#pragma unroll
+      for (int j = 1; j < NA; ++j) v += acc[j][nt][e];
+      s[nt][e] = v;
+    }
+}
+
+// O^T += V^T P^T for one page: FP8 cache.  Pair row p (slots 2p, 2p+1) is
+// [256 dims][2 bytes] at box rows 32 + 4p .. 32 + 4p + 3; two bytes are the
+// (token 2p, token 2p+1) pair an A register holds.  Thread (gid, tig) covers
+// dims 16*gid + mt (rows gid of m-tile mt) and 128 + 16*gid + mt (rows
+// gid+8), pairs tig and tig+4, as in the NVFP4 path.  Tokens at or past
+// page_lim (a partial or missing page) are zeroed, so stale codes cannot
+// reach the product.
+template <int NTW>
+__device__ __forceinline__ void pv_fp8(uint32_t sb, int lane, WarpState<NTW>& st,
+                                       const uint32_t (&pb)[NTW][2], int page_lim) {
+  const int gid = lane >> 2, tig = lane & 3;
+  auto keep = [&](int t) -> uint32_t {
+    return (t < page_lim ? 0x0000FFFFu : 0u) | (t + 1 < page_lim ? 0xFFFF0000u : 0u);
+  };
+  const uint32_t ma = keep(2 * tig), mb = keep(2 * tig + 8);
+  // dims 16*gid .. +15 of pair p, low half (dims 0..127) and high half
+  auto ld2 = [&](int p, int hi, uint4& x0, uint4& x1) {
+    const int row = 32 + 4 * p + 2 * hi + (gid >> 2);
+    x0 = lds128(sb + swz128(row, 32 * (gid & 3)));
+    x1 = lds128(sb + swz128(row, 32 * (gid & 3) + 16));
+  };
+  uint4 al0, al1, ah0, ah1, bl0, bl1, bh0, bh1;
+  ld2(tig, 0, al0, al1);
+  ld2(tig, 1, ah0, ah1);
+  ld2(tig + 4, 0, bl0, bl1);
+  ld2(tig + 4, 1, bh0, bh1);
+  const uint32_t wal[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+  const uint32_t wah[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+  const uint32_t wbl[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
+  const uint32_t wbh[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) {  // word wi: dims 16*gid + 2wi, +1
+    uint32_t a0[2], a1[2], a2[2], a3[2];
+    e4m3x4_to_f16x2x2(wal[wi], a0[0], a0[1]);
+    e4m3x4_to_f16x2x2(wah[wi], a1[0], a1[1]);
+    e4m3x4_to_f16x2x2(wbl[wi], a2[0], a2[1]);
+    e4m3x4_to_f16x2x2(wbh[wi], a3[0], a3[1]);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int mt = 2 * wi + u;
+      const uint32_t af[4] = {a0[u] & ma, a1[u] & ma, a2[u] & mb, a3[u] & mb};
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pb[nt][0], pb[nt][1]);
     }
@@ -823,13 +922,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
       uint32_t pb[NP][NTW][2];
 #pragma unroll
       for (int pg = 0; pg < NP; ++pg) {
-        if (KVDT == PNKV_KV_NVFP4) qk_nvfp4<NTW>(sb[pg], lane, qf, sacc[pg]);
+        if constexpr (KVDT == PNKV_KV_NVFP4) qk_nvfp4<NTW>(sb[pg], lane, qf, sacc[pg]);
+        else if constexpr (KVDT == PNKV_KV_FP8) qk_fp8<NTW>(sb[pg], lane, qf, sacc[pg]);
         else qk_bf16<NTW>(sb[pg], lane, qf, sacc[pg]);
       }
       softmax_pages<NTW, NP>(st, sacc, a.qk_scale_log2, key0, page_lim, masked, lane, pb);
 #pragma unroll
       for (int pg = 0; pg < NP; ++pg) {
-        if (KVDT == PNKV_KV_NVFP4) pv_nvfp4<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
+        if constexpr (KVDT == PNKV_KV_NVFP4) pv_nvfp4<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
+        else if constexpr (KVDT == PNKV_KV_FP8) pv_fp8<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
         else pv_bf16<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
       }
       __syncwarp();
@@ -885,7 +986,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
               int d;
               float2 v;
               const float w = wgt[nt][c];
-              if (KVDT == PNKV_KV_NVFP4) {
+              if (KVDT != PNKV_KV_BF16) {
                 const int mt = j & ~1;
                 const int e = (j & 1) ? c + 2 : c;
                 d = ((j & 1) ? 128 : 0) + 16 * gid + mt;
@@ -970,7 +1071,7 @@ int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
   // warps per CTA: NVFP4 stages are small, so many consumer streams each keep
   // two or more stages; bf16 stages are 16 KiB, so fewer streams share the
   // 13 that fit and each still double-buffers.
-  constexpr bool fp4 = KVDT == PNKV_KV_NVFP4;
+  constexpr bool fp4 = KVDT != PNKV_KV_BF16;  // coded pools (NVFP4, FP8): small stages
 #ifndef PNKV_NVFP4_NW
 #define PNKV_NVFP4_NW 12
 #define PNKV_NVFP4_QS 0
@@ -1052,9 +1153,9 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   a.num_pages = cache->num_pages;
   a.hkv = cache->num_kv_heads;
   a.group = group;
-  const float kscale = cache->dtype == PNKV_KV_NVFP4 ? cache->k_scale : 1.0f;
+  const float kscale = cache->dtype != PNKV_KV_BF16 ? cache->k_scale : 1.0f;
   a.qk_scale_log2 = sm_scale * kscale * kLog2e;
-  a.out_scale = cache->dtype == PNKV_KV_NVFP4 ? cache->v_scale : 1.0f;
+  a.out_scale = cache->dtype != PNKV_KV_BF16 ? cache->v_scale : 1.0f;
   a.q = q_roped;
   a.qo_indptr = qo_indptr;
   a.page_table = page_table;
@@ -1073,9 +1174,11 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
 
   CUtensorMap map;
   const int box_rows = cache->dtype == PNKV_KV_NVFP4 ? Geometry<PNKV_KV_NVFP4>::kBoxRows
+                       : cache->dtype == PNKV_KV_FP8 ? Geometry<PNKV_KV_FP8>::kBoxRows
                                                      : Geometry<PNKV_KV_BF16>::kBoxRows;
   if ((st = make_pool_map(cache, box_rows, &map)) != PNKV_OK) return st;
   cudaStream_t s = as_stream(stream);
   if (cache->dtype == PNKV_KV_NVFP4) return dispatch_rows<PNKV_KV_NVFP4>(map, a, grid, s);
+  if (cache->dtype == PNKV_KV_FP8) return dispatch_rows<PNKV_KV_FP8>(map, a, grid, s);
   return dispatch_rows<PNKV_KV_BF16>(map, a, grid, s);
 }

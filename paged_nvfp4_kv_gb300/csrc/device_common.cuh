@@ -131,6 +131,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return out;
 }
 
+// Four E4M3 bytes as two fp16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi; the
+// lower byte of each pair in the lower half).  Exact: every E4M3 value is an
+// fp16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // fp32 -> E4M3 byte, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float x) {
   uint16_t out;

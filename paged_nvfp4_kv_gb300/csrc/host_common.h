@@ -55,9 +55,10 @@ inline int check_cache(const pnkv_cache* c) {
   if (!c || !c->pool || c->num_pages <= 0 || c->page_size != 16 || c->head_dim != 256 ||
       c->num_kv_heads < 1 || c->num_kv_heads > 16)
     return PNKV_ERR_INVALID_ARG;
-  if (c->dtype != PNKV_KV_BF16 && c->dtype != PNKV_KV_NVFP4) return PNKV_ERR_INVALID_ARG;
+  if (c->dtype != PNKV_KV_BF16 && c->dtype != PNKV_KV_NVFP4 && c->dtype != PNKV_KV_FP8)
+    return PNKV_ERR_INVALID_ARG;
   if (!aligned(c->pool, 128)) return PNKV_ERR_INVALID_ARG;
-  if (c->dtype == PNKV_KV_NVFP4) {
+  if (c->dtype != PNKV_KV_BF16) {
     if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || !std::isfinite(c->k_scale) ||
         !std::isfinite(c->v_scale))
       return PNKV_ERR_INVALID_ARG;
@@ -67,7 +68,9 @@ inline int check_cache(const pnkv_cache* c) {
 
 // Bytes of one KV head's record inside a page (head_dim 256, 16 slots).
 inline int64_t head_record_bytes(int dtype) {
-  return dtype == PNKV_KV_NVFP4 ? 2 * 16 * (128 + 16) : 2 * 16 * 256 * 2;
+  if (dtype == PNKV_KV_NVFP4) return 2 * 16 * (128 + 16);
+  if (dtype == PNKV_KV_FP8) return 2 * 16 * 256;
+  return 2 * 16 * 256 * 2;
 }
 
 }  // namespace pnkv

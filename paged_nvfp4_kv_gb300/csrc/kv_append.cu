@@ -1,5 +1,5 @@
 // kv_append_nvfp4: fused rope + quantise + page scatter for the step's new
-// tokens.
+// tokens (NVFP4, FP8 or bf16 pools).
 //
 // Rope with the YaRN table, mscale already inside cos/sin ("A 1,048,576-token
 // context on two RTX 5090s", section "YaRN, and matching what vLLM actually
@@ -8,7 +8,11 @@
 // section "Why NVFP4 KV changes the math": E2M1 codes with an FP8 E4M3 scale
 // per 16 elements and one fp32 scale per tensor).  Every fp32 step is one
 // IEEE operation with round-to-nearest (no contraction into FMAs), so the
-// bytes written are a pure function of the inputs.
+// bytes written are a pure function of the inputs.  An FP8 pool (the fp8 KV
+// cache of the comparison engine in "A 1,048,576-token context on two RTX
+// 5090s", section "Against vLLM: prefill loses, decode wins, and one
+// surprise") stores E4M3(x * fp32(1/g)) per element with one scale g per
+// tensor.
 //
 // One warp per (token, head) row of 256 elements: lane l owns elements
 // 8l .. 8l+7 (one 16-byte load).  Rope partners (j, j + R/2) sit R/16 lanes
@@ -57,6 +61,13 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
   uint32_t c = (m > 0.25f) + (m >= 0.75f) + (m > 1.25f) + (m >= 1.75f) + (m > 2.5f) + (m >= 3.5f) +
                (m > 5.0f);
   return c | ((__float_as_uint(y) >> 31) << 3);
+}
+
+// E4M3 code of a binary32 value: round to nearest even, saturate at 448; the
+// sign bit is the value's (tiny negatives give code 0x80 whatever the
+// conversion does with the sign of a zero result).
+__device__ __forceinline__ uint32_t e4m3_code(float y) {
+  return (f32_to_e4m3_satfinite(y) & 0xFFu) | ((__float_as_uint(y) >> 31) << 7);
 }
 
 // Quantise this lane's 8 elements (part of the 16-element block shared with
@@ -185,6 +196,20 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
     if (a.dtype == PNKV_KV_BF16) {
       reinterpret_cast<uint4*>(rec + slot * 512)[lane] = pack_bf16x8(kx);
       reinterpret_cast<uint4*>(rec + 8192 + slot * 512)[lane] = vraw;
+    } else if (a.dtype == PNKV_KV_FP8) {
+      // K codes [16][256]: bytes 8*lane .. +7 of the slot's row; V codes
+      // [8 pairs][256][2]: byte 2d + (slot odd) of the pair's row
+      const float rk = __frcp_rn(a.k_scale), rv = __frcp_rn(a.v_scale);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lo |= e4m3_code(__fmul_rn(kx[e], rk)) << (8 * e);
+        hi |= e4m3_code(__fmul_rn(kx[e + 4], rk)) << (8 * e);
+      }
+      reinterpret_cast<uint2*>(rec + slot * 256)[lane] = make_uint2(lo, hi);
+      uint8_t* vrow = rec + 4096 + (slot >> 1) * 512 + (slot & 1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vrow[2 * (8 * lane + e)] = static_cast<uint8_t>(e4m3_code(__fmul_rn(vx[e], rv)));
     } else {
       uint32_t ks, vs;
       const uint32_t kc = quantize8(kx, a.k_scale, &ks);
@@ -220,8 +245,8 @@ extern "C" int kv_append_nvfp4(const pnkv_cache* cache, const int32_t* page_tabl
   using namespace pnkv;
   int st = check_cache(cache);
   if (st != PNKV_OK) return st;
-  if (cache->dtype == PNKV_KV_NVFP4) {
-    // keep d = E4M3(S) * g and 1/d normal binary32 numbers
+  if (cache->dtype != PNKV_KV_BF16) {
+    // keep d = E4M3(S) * g (NVFP4), 1/g (FP8) and 1/d normal binary32 numbers
     const float lo = 7.8886091e-31f, hi = 1.2676506e30f;  // 2^-100, 2^100
     if (cache->k_scale < lo || cache->k_scale > hi || cache->v_scale < lo || cache->v_scale > hi)
       return PNKV_ERR_INVALID_ARG;

@@ -253,13 +253,6 @@ __device__ bool find_tile(const PrefillArgs& a, int64_t idx, Tile* t) {
   return false;
 }
 
-// Four E4M3 bytes as two fp16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi).
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h; }"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
 // Parity of the phase in which item g of a ring of n slots lands in its slot.
 __device__ __forceinline__ uint32_t ring_parity(int64_t g, int n) { return static_cast<uint32_t>((g / n) & 1); }
 

@@ -93,6 +93,15 @@ def test_million_token_decode_full():
     _check(w, s, o32, o16, rows, {0: _pages_of(w, 0, np.random.default_rng(3))})
 
 
+def test_million_token_decode_fp8_full():
+    """The million-token decode with an FP8 (E4M3, per-tensor scale) pool."""
+    from paged_nvfp4_kv_gb300 import workloads as W
+    w = W.million_token_decode_fp8()
+    s, o32, o16 = _run(w)
+    rows = [(0, h) for h in (4, 11, 19)]
+    _check(w, s, o32, o16, rows, {0: _pages_of(w, 0, np.random.default_rng(7))})
+
+
 def test_multi_session_verify_full():
     from paged_nvfp4_kv_gb300 import workloads as W
     w = W.multi_session_verify()

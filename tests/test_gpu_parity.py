@@ -64,6 +64,12 @@ CASES = {
     "long-nvfp4": ("nvfp4", [70000, 7000], [1, 1]),
     "long-verify5-nvfp4": ("nvfp4", [40000, 23000], [5, 5]),
     "long-verify5-bf16": ("bf16", [30000], [5]),
+    # FP8 (E4M3, per-tensor scale) pools through the same entry points
+    "ragged-fp8": ("fp8", [1000, 36, 4100], [1, 1, 1]),
+    "verify5-fp8": ("fp8", [700, 50, 333, 2011], [5, 5, 5, 5]),
+    "qlen8-fp8": ("fp8", [300, 1800], [8, 3]),
+    "page-edge-fp8": ("fp8", [16, 15, 17, 31, 32, 0], [1, 1, 1, 1, 1, 1]),
+    "long-fp8": ("fp8", [70000, 7000], [1, 1]),
     # more than 64 query rows per KV head: the tensor-core tile path
     "prefill-nvfp4": ("nvfp4", [3000, 500, 77], [100, 37, 1]),
     "prefill-long-nvfp4": ("nvfp4", [40000], [300]),
@@ -148,3 +154,18 @@ def test_page_permutation_invariance():
     again = s.attend(out_fp32=True).clone()
     torch.cuda.synchronize()
     assert torch.equal(again.view(torch.int32), out32.view(torch.int32))
+
+
+def test_fp8_prefill_chunk_is_unsupported():
+    """More than 64 query rows per KV head run the tensor-core tile, built for
+    NVFP4 pools only: an FP8 pool gets PNKV_ERR_UNSUPPORTED, nothing runs."""
+    from paged_nvfp4_kv_gb300 import _lib
+    from paged_nvfp4_kv_gb300.engine import DecodeSession
+    w = _workload("fp8-chunk", "fp8", [500], [20])
+    s = DecodeSession(w)
+    s.fill()
+    s.append()
+    with pytest.raises(RuntimeError, match="unsupported"):
+        s.attend(out_fp32=True)
+    torch.cuda.synchronize()
+    assert s.error_word() == 0

@@ -20,7 +20,8 @@ Sources, cited by page title and section:
   and "The stack, for the impatient".
 * "A 1,048,576-token context on two RTX 5090s", section "Against vLLM:
   prefill loses, decode wins, and one surprise" (the comparison engine's fp8
-  KV cache).
+  KV cache); the README's sections "Dual-GPU (TP2) and YaRN 1M context" and
+  "Memory, per GPU" (INT8 group-64 KV).
 * The published YaRN method (Peng et al., 2023, "YaRN: Efficient Context
   Window Extension of Large Language Models"), which the first page cites as
   its reference 3, for the NTK-by-parts ramp and the attention temperature.
@@ -32,6 +33,7 @@ Modules:
   yarn       YaRN inverse frequencies, mscale, cos/sin tables, rope.
   nvfp4      two-level NVFP4 block quantise / dequantise.
   fp8        per-tensor FP8 (E4M3) quantise / dequantise.
+  int8       INT8 group-64 quantise / dequantise (fp16 group scales).
   paged      page-pool byte layout, scatter and gather.
   attention  dense and paged attention, split-KV partials, LSE combine.
 

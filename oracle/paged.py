@@ -27,19 +27,43 @@ Inside a page the record of each KV head h is contiguous, heads in order:
     V codes   [8 slot pairs][D][2]    bytes 2d, 2d+1 of pair i: element d
                                       of slots 2i, 2i+1 (the same pairing as
                                       NVFP4, one byte per element)
+  INT8 group-64 (8,448 bytes per page-head; int8 codes, fp16 scale per 64
+  contiguous elements of a slot):
+    K codes   [16 slots][D bytes]     dim d at byte 64*((d%16)//4) + 4*(d//16)
+                                      + d%4 of the slot's row (the 64 bytes a
+                                      tensor-core lane quarter reads for its
+                                      16 k-steps are contiguous)
+    K scales  [16 slots][D/64] fp16
+    V codes   [8 slot pairs][D][2]    position p = 32*(d%8) + d//8 holds dim d;
+                                      bytes 2p, 2p+1 of pair i: element d of
+                                      slots 2i, 2i+1
+    V scales  [16 slots][D/64] fp16
   bf16 (16,384 bytes per page-head):
     K [16 slots][D] bf16 (little-endian), then V [16 slots][D] bf16
 """
 import numpy as np
 
-from . import fp8
+from . import fp8, int8
 from .formats import bf16_bits, bf16_from_bits
 from .nvfp4 import dequantize, pack_nibbles, quantize, unpack_nibbles
 
 PAGE = 16
 NVFP4 = "nvfp4"
 FP8 = "fp8"
+INT8 = "int8"
 BF16 = "bf16"
+
+
+def int8_k_position(d):
+    """Byte of a slot's K row holding dim d (INT8 pages)."""
+    d = np.asarray(d)
+    return 64 * ((d % 16) // 4) + 4 * (d // 16) + d % 4
+
+
+def int8_v_position(d):
+    """Position (2-byte pair) of a pair row holding dim d (INT8 pages)."""
+    d = np.asarray(d)
+    return 32 * (d % 8) + d // 8
 
 
 def page_head_bytes(dtype, head_dim):
@@ -47,6 +71,8 @@ def page_head_bytes(dtype, head_dim):
         return 2 * PAGE * (head_dim // 2 + head_dim // 16)
     if dtype == FP8:
         return 2 * PAGE * head_dim
+    if dtype == INT8:
+        return 2 * PAGE * (head_dim + 2 * (head_dim // int8.GROUP))
     return 2 * PAGE * head_dim * 2
 
 
@@ -66,6 +92,13 @@ def _sections(dtype, head_dim):
         return (k0, cb), (ks, sb), (v0, head_dim), (vs, sb)
     if dtype == FP8:
         return (0, head_dim), None, (PAGE * head_dim, 2 * head_dim), None
+    if dtype == INT8:
+        sb = 2 * (head_dim // int8.GROUP)
+        k0 = 0
+        ks = PAGE * head_dim
+        v0 = ks + PAGE * sb
+        vs = v0 + PAGE * head_dim
+        return (k0, head_dim), (ks, sb), (v0, 2 * head_dim), (vs, sb)
     rb = head_dim * 2
     return (0, rb), None, (PAGE * rb, rb), None
 
@@ -90,6 +123,13 @@ def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, 
     elif dtype == FP8:
         krow = fp8.quantize(k, g_k)
         vq = fp8.quantize(v, g_v)
+    elif dtype == INT8:
+        kq, kscale = int8.quantize(k)
+        vq, vscale = int8.quantize(v)
+        krow = np.zeros(kq.shape, np.uint8)
+        krow[..., int8_k_position(np.arange(head_dim))] = kq.view(np.uint8)
+        kscale, vscale = kscale.view(np.uint8), vscale.view(np.uint8)   # little-endian fp16
+        vpos = int8_v_position(np.arange(head_dim))
     else:
         krow = bf16_bits(k).view(np.uint8).reshape(k.shape[0], num_kv_heads, -1)
         vrow = bf16_bits(v).view(np.uint8).reshape(v.shape[0], num_kv_heads, -1)
@@ -114,6 +154,12 @@ def scatter_tokens(pool, dtype, num_kv_heads, head_dim, page_table, seq_of_tok, 
                 # byte 2d + (slot odd) of the pair's row
                 row0 = base + v0 + (slot // 2) * vb + (slot % 2)
                 pool[page, row0: row0 + vb: 2] = vq[t, h]
+            elif dtype == INT8:
+                # byte 2 p(d) + (slot odd) of the pair's row
+                pool[page, base + v0 + (slot // 2) * vb + 2 * vpos + (slot % 2)] = vq[t, h].view(np.uint8)
+                (ko, ksb), (vo, vsb) = ks, vs
+                pool[page, base + ko + slot * ksb: base + ko + (slot + 1) * ksb] = kscale[t, h].reshape(-1)
+                pool[page, base + vo + slot * vsb: base + vo + (slot + 1) * vsb] = vscale[t, h].reshape(-1)
             else:
                 pool[page, base + v0 + slot * vb: base + v0 + (slot + 1) * vb] = vrow[t, h]
     return pool
@@ -136,6 +182,15 @@ def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, sta
     elif dtype == FP8:
         krow = fp8.quantize(k, g_k)
         vq = fp8.quantize(v, g_v)
+    elif dtype == INT8:
+        kq, kscale = int8.quantize(k)
+        vq, vscale = int8.quantize(v)
+        krow = np.zeros(kq.shape, np.uint8)
+        krow[..., int8_k_position(np.arange(head_dim))] = kq.view(np.uint8)
+        kscale = kscale.view(np.uint8).reshape(T, num_kv_heads, -1)
+        vscale = vscale.view(np.uint8).reshape(T, num_kv_heads, -1)
+        vq = vq.view(np.uint8)
+        vpos = int8_v_position(np.arange(head_dim))
     else:
         krow = bf16_bits(k).view(np.uint8).reshape(T, num_kv_heads, -1)
         vrow = bf16_bits(v).view(np.uint8).reshape(T, num_kv_heads, -1)
@@ -162,6 +217,13 @@ def scatter_sequence_fast(pool, dtype, num_kv_heads, head_dim, pages_of_seq, sta
         elif dtype == FP8:
             for d in range(head_dim):
                 pool[pages, base + v0 + (slots // 2) * vb + 2 * d + (slots % 2)] = vq[:, h, d]
+        elif dtype == INT8:
+            for d in range(head_dim):
+                pool[pages, base + v0 + (slots // 2) * vb + 2 * vpos[d] + (slots % 2)] = vq[:, h, d]
+            (ko, ksb), (vo, vsb) = ks, vs
+            for j in range(ksb):
+                pool[pages, base + ko + slots * ksb + j] = kscale[:, h, j]
+                pool[pages, base + vo + slots * vsb + j] = vscale[:, h, j]
         else:
             for j in range(vb):
                 pool[pages, base + v0 + slots * vb + j] = vrow[:, h, j]
@@ -195,6 +257,18 @@ def gather_sequence(pool, dtype, num_kv_heads, head_dim, pages_of_seq, seq_len, 
         vcols = (base + v0 + (slots[:, None] // 2) * vb + 2 * np.arange(head_dim)[None, :]
                  + (slots % 2)[:, None])
         return fp8.dequantize(krow, g_k), fp8.dequantize(pool[pages[:, None], vcols], g_v)
+    if dtype == INT8:
+        (ko, ksb), (vo, vsb) = ks, vs
+        dims = np.arange(head_dim)
+        kq = krow[:, int8_k_position(dims)].view(np.int8)
+        vcols = (base + v0 + (slots[:, None] // 2) * vb + 2 * int8_v_position(dims)[None, :]
+                 + (slots % 2)[:, None])
+        vq = pool[pages[:, None], vcols].view(np.int8)
+        kscol = base + ko + slots[:, None] * ksb + np.arange(ksb)[None, :]
+        vscol = base + vo + slots[:, None] * vsb + np.arange(vsb)[None, :]
+        ksc = np.ascontiguousarray(pool[pages[:, None], kscol]).view(np.uint16)
+        vsc = np.ascontiguousarray(pool[pages[:, None], vscol]).view(np.uint16)
+        return int8.dequantize(kq, ksc), int8.dequantize(vq, vsc)
     vcols = base + v0 + slots[:, None] * vb + np.arange(vb)[None, :]
     vrow = pool[pages[:, None], vcols]
     kk = bf16_from_bits(krow.view(np.uint16))

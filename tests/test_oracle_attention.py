@@ -150,7 +150,7 @@ def test_bf16_page_layout_offsets_by_hand():
     assert np.count_nonzero(pool) == 3
 
 
-@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.FP8, PG.BF16])
+@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.FP8, PG.INT8, PG.BF16])
 def test_scatter_gather_roundtrip_and_fast_path(dtype):
     rng = np.random.default_rng(27)
     L, H = 70, 4
@@ -172,7 +172,7 @@ def test_scatter_gather_roundtrip_and_fast_path(dtype):
             assert np.corrcoef(kk.ravel(), k[:, h].ravel())[0, 1] > 0.98
 
 
-@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.FP8, PG.BF16])
+@pytest.mark.parametrize("dtype", [PG.NVFP4, PG.FP8, PG.INT8, PG.BF16])
 def test_paged_decode_matches_dense_and_is_permutation_invariant(dtype):
     rng = np.random.default_rng(28)
     H, G, lens, qlen = 2, 3, [40, 23], [1, 5]

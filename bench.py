@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 METRIC = "1M-ctx paged decode attention: KV tokens/s/layer and HBM GB/s (% of GB300 peak)"
 UNIT = "KV tokens/s/layer"
 FALLBACK_HBM_GBS = 6800.0   # earlier GB300 copy measurement, used if no measured peaks file
-ALGO_BYTES_PER_TOKEN = {"nvfp4": 4 * 2 * (128 + 16), "fp8": 4 * 2 * 256, "bf16": 4 * 2 * 256 * 2}
+ALGO_BYTES_PER_TOKEN = {"nvfp4": 4 * 2 * (128 + 16), "fp8": 4 * 2 * 256, "int8": 4 * 2 * (256 + 8),
+                        "bf16": 4 * 2 * 256 * 2}
 
 
 def parse():
@@ -41,7 +42,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", type=int, default=3,
-                   help="workload number: 1..5 as in the workload table, 6 = reduced chunked prefill (profiling)")
+                   help="workload number: 1..5 as in the workload table, 6 = reduced chunked prefill "
+                        "(profiling), 7/8 = the million-token decode with an FP8/INT8 cache")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     return p.parse_args()
@@ -183,7 +185,7 @@ def oracle_rate(w, seconds, max_keys=None):
     from oracle import yarn as OY
 
     L = int(w.seq_lens[0])
-    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "bf16": OP.BF16}[w.kv_dtype]
+    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "int8": OP.INT8, "bf16": OP.BF16}[w.kv_dtype]
     R = w.yarn["rotary_dim"]
 
     def run(n):

@@ -75,9 +75,12 @@ enum {
   PNKV_KV_BF16 = 0,  /* K, V stored as bf16                                  */
   PNKV_KV_NVFP4 = 1, /* E2M1 codes + E4M3 scale per 16 elements + fp32
                         per-tensor scale ([NVFP4-page])                      */
-  PNKV_KV_FP8 = 2    /* E4M3 codes + fp32 per-tensor scale (the comparison
+  PNKV_KV_FP8 = 2,   /* E4M3 codes + fp32 per-tensor scale (the comparison
                         engine's fp8 cache, [YaRN-page] section "Against
                         vLLM: prefill loses, decode wins, and one surprise") */
+  PNKV_KV_INT8 = 3   /* int8 codes + fp16 scale per 64 elements ([TP2-README]
+                        "Dual-GPU (TP2) and YaRN 1M context", "Memory, per
+                        GPU": the million-token cache)                      */
 };
 
 /* YaRN parameters ([YaRN-paper], NTK-by-parts; [YaRN-page]; [TP2-README]).
@@ -116,26 +119,37 @@ typedef struct {
  *     K codes  [16 slots][256 B]  E4M3, element d of a slot at byte d
  *     V codes  [8 slot pairs][256][2 B]  bytes 2d, 2d+1 of pair i: element
  *                                  d of slots 2i and 2i+1
+ *   INT8 group-64, head_dim 256 (8,448 bytes):
+ *     K codes  [16 slots][256 B]  int8; dim d at byte 64*((d%16)/4) +
+ *                                  4*(d/16) + d%4 of the slot's row
+ *     K scales [16 slots][4] fp16 (one per 64 contiguous dims)
+ *     V codes  [8 slot pairs][256][2 B]  position p = 32*(d%8) + d/8 holds
+ *                                  dim d; bytes 2p, 2p+1 of pair i: element
+ *                                  d of slots 2i and 2i+1
+ *     V scales [16 slots][4] fp16
  *   bf16, head_dim 256 (16,384 bytes):
  *     K [16 slots][256] bf16, then V [16 slots][256] bf16
- * A page is num_kv_heads * record bytes (18,432 B NVFP4, 32,768 B FP8 or
- * 65,536 B bf16 for 4 KV heads).  `pool` must be 128-byte aligned.
+ * A page is num_kv_heads * record bytes (18,432 B NVFP4, 32,768 B FP8,
+ * 33,792 B INT8 or 65,536 B bf16 for 4 KV heads).  `pool` must be 128-byte
+ * aligned.
  *
  * NVFP4 decode of element i of a block with scale byte S: E2M1(code_i) *
  * E4M3(S) * k_scale (K) or * v_scale (V); k_scale and v_scale are the
  * per-tensor fp32 decode scales, calibrated by the caller.  FP8 decode:
  * E4M3(code) * k_scale (or v_scale); the encoder writes E4M3_rn_satfinite(x *
  * fp32(1/scale)).  FP8 precondition: bytes of slots not written yet hold no
- * E4M3 NaN code (0x7F, 0xFF); a zero-filled pool satisfies it. */
+ * E4M3 NaN code (0x7F, 0xFF); a zero-filled pool satisfies it.  INT8 decode:
+ * code * fp16 group scale (k_scale and v_scale are not used). */
 typedef struct {
   void* pool;            /* device, num_pages * page bytes                   */
   int64_t num_pages;
   int32_t page_size;     /* must be 16                                       */
   int32_t num_kv_heads;  /* 1..16                                            */
   int32_t head_dim;      /* must be 256                                      */
-  int32_t dtype;         /* PNKV_KV_BF16, PNKV_KV_NVFP4 or PNKV_KV_FP8       */
+  int32_t dtype;         /* PNKV_KV_BF16, _NVFP4, _FP8 or _INT8              */
   float k_scale;         /* NVFP4/FP8: per-tensor K decode scale (> 0)       */
   float v_scale;         /* NVFP4/FP8: per-tensor V decode scale (> 0)       */
+                         /* (INT8 and bf16 pools ignore both)                */
 } pnkv_cache;
 
 /* Bytes of one page of `cache` (written to *out).  Host only. */
@@ -173,7 +187,9 @@ int yarn_rope_tables(const pnkv_yarn_params* params, int64_t max_pos,
  *   r = fp32(1 / d), code_i = E2M1_rn_satfinite(fp32(x_i * r)), the sign of
  *   a value that rounds to zero kept (g = k_scale for K, v_scale for V);
  * or FP8: code_i = E4M3_rn_satfinite(fp32(x_i * fp32(1 / g))), the sign of a
- * value that rounds to zero kept.  (The name keeps the NVFP4 path's; the
+ * value that rounds to zero kept; or INT8: per 64-element group a = max |x|,
+ * s = fp16_rn_satfinite(fp32(a / 127)), zero group if s == 0, else code_i =
+ * clamp(RNE(fp32(x_i * fp32(1 / s))), -127, 127).  (The name keeps the NVFP4 path's; the
  * pool's dtype selects the encoder.)  NVFP4 and FP8 scales must lie in
  * [2^-100, 2^100].
  *
@@ -217,7 +233,7 @@ int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads);
  * With causal != 0, query row j of sequence b sees keys 0 .. seq_lens[b] -
  * qlen_b + j; otherwise all seq_lens[b] keys.  Logits are
  * z = (q . k) * sm_scale with q the roped bf16 query and k, v the cache
- * values (NVFP4, FP8: dequantised), softmax in fp32 with fp16 probabilities in
+ * values (NVFP4, FP8, INT8: dequantised), softmax in fp32 with fp16 probabilities in
  * the P.V product.  Each split writes its normalised partial output and
  * natural-log LSE; empty splits write LSE = -inf.
  *
@@ -234,10 +250,10 @@ int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads);
  *               where each (sequence, KV head)'s partials are; read by
  *               split_kv_combine
  *   dev_err     device int32 word
- * The pool must hold NVFP4, FP8 or bf16 pages with head_dim 256 and 16-token
- * pages; num_q_heads / num_kv_heads in 1..8 rows per query token.  More than
- * 64 rows per KV head (a prefill chunk) run the tensor-core tile, built for
- * NVFP4 pools; FP8 and bf16 pools return PNKV_ERR_UNSUPPORTED there. */
+ * The pool must hold NVFP4, FP8, INT8 or bf16 pages with head_dim 256 and
+ * 16-token pages; num_q_heads / num_kv_heads in 1..8 rows per query token.
+ * More than 64 rows per KV head (a prefill chunk) run the tensor-core tile,
+ * built for NVFP4 pools; other pools return PNKV_ERR_UNSUPPORTED there. */
 int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q_roped,
                            const int32_t* qo_indptr, const int32_t* page_table,
                            int64_t pt_stride, const int32_t* seq_lens,

@@ -10,13 +10,13 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import PNKV_KV_BF16, PNKV_KV_FP8, PNKV_KV_NVFP4, CacheDesc, YarnParams
+from ._lib import PNKV_KV_BF16, PNKV_KV_FP8, PNKV_KV_INT8, PNKV_KV_NVFP4, CacheDesc, YarnParams
 
 __all__ = ["Cache", "YarnParams", "yarn_params", "yarn_rope_tables", "kv_append_nvfp4",
            "paged_decode_attention", "split_kv_combine", "decode_slots", "work_meta_ints",
-           "page_bytes", "PNKV_KV_BF16", "PNKV_KV_NVFP4", "PNKV_KV_FP8", "decode_dev_err"]
+           "page_bytes", "PNKV_KV_BF16", "PNKV_KV_NVFP4", "PNKV_KV_FP8", "PNKV_KV_INT8", "decode_dev_err"]
 
-_DTYPES = {"bf16": PNKV_KV_BF16, "nvfp4": PNKV_KV_NVFP4, "fp8": PNKV_KV_FP8}
+_DTYPES = {"bf16": PNKV_KV_BF16, "nvfp4": PNKV_KV_NVFP4, "fp8": PNKV_KV_FP8, "int8": PNKV_KV_INT8}
 
 
 def _ptr(t):
@@ -39,7 +39,8 @@ class Cache:
     """A paged KV pool (one layer) and its C descriptor.
 
     ``pool`` is a caller-owned uint8 device tensor of num_pages * page bytes;
-    ``k_scale``/``v_scale`` are the NVFP4 or FP8 per-tensor decode scales."""
+    ``k_scale``/``v_scale`` are the NVFP4 or FP8 per-tensor decode scales
+    (INT8 pools carry their scales per 64-element group and ignore them)."""
 
     def __init__(self, num_pages, dtype="nvfp4", num_kv_heads=4, head_dim=256, k_scale=1.0,
                  v_scale=1.0, pool=None, device="cuda"):

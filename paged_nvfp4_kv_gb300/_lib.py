@@ -17,6 +17,7 @@ PNKV_ERR_CUDA = -3
 PNKV_KV_BF16 = 0
 PNKV_KV_NVFP4 = 1
 PNKV_KV_FP8 = 2
+PNKV_KV_INT8 = 3
 
 DEV_ERR_BITS = {1: "page id", 2: "position", 4: "seq_len", 8: "qo_indptr", 16: "timeout",
                 32: "seq index"}

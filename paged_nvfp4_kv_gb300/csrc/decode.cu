@@ -70,7 +70,7 @@ struct DecodeArgs {
   int32_t hkv;
   int32_t group;          // query heads per KV head
   float qk_scale_log2;    // sm_scale * log2(e) (* k_scale for NVFP4 and FP8)
-  float out_scale;        // v_scale for NVFP4 and FP8, 1 for bf16
+  float out_scale;        // v_scale for NVFP4 and FP8, 1 for INT8 and bf16
   const uint16_t* q;      // roped bf16 queries [total_q, hq, 256]
   const int32_t* qo_indptr;
   const int32_t* page_table;
@@ -101,6 +101,12 @@ struct Geometry<PNKV_KV_FP8> {
   static constexpr int kBoxRows = 64;      // 8,192 B head record
   static constexpr int kStageBytes = 8192;
   static constexpr uint32_t kTxBytes = 8192;
+};
+template <>
+struct Geometry<PNKV_KV_INT8> {
+  static constexpr int kBoxRows = 66;      // 8,448 B head record
+  static constexpr int kStageBytes = 9216; // next multiple of 1,024
+  static constexpr uint32_t kTxBytes = 8448;
 };
 template <>
 struct Geometry<PNKV_KV_BF16> {
@@ -340,7 +346,19 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, const Piece& pc, int
   for (int nt = 0; nt < NTW; ++nt) {
     const int n = row_base + 8 * nt + gid;
     const int rows = a.group * pc.s.qlen;
-    if (n < rows) {
+    if (KVDT == PNKV_KV_INT8 && n < rows) {
+      // INT8 k order: k-step kk holds dims 16*kk + 4*tig + 0..3 (one 64-dim
+      // scale group per four k-steps)
+      const int t = pc.s.q0 + n / a.group;
+      const int hq = pc.h * a.group + n % a.group;
+      const uint2* src = reinterpret_cast<const uint2*>(a.q + (static_cast<int64_t>(t) * a.hq + hq) * 256 + 4 * tig);
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const uint2 w = __ldg(src + 4 * kk);
+        qb[nt][kk][0] = f32x2_to_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+        qb[nt][kk][1] = f32x2_to_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      }
+    } else if (n < rows) {
       const int t = pc.s.q0 + n / a.group;
       const int hq = pc.h * a.group + n % a.group;
       const uint4* src = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(t) * a.hq + hq) * 256 +
@@ -684,6 +702,111 @@ __device__ __forceinline__ void pv_fp8(uint32_t sb, int lane, WarpState<NTW>& st
   }
 }
 
+// S^T for one page: INT8 group-64 cache.  Token t's codes are box rows 2t,
+// 2t+1 with dims permuted so that lane (gid, tig) reads its 16 k-steps
+// (dims 16*kk + 4*tig .. +3) as 64 contiguous bytes: chunk c of them is scale
+// group c.  Each group's four MMAs go to a fresh accumulator that is then
+// scaled by the two tokens' group scales (fp32 FFMA), so the int8 codes enter
+// the product exactly.
+template <int NTW, typename Q>
+__device__ __forceinline__ void qk_int8(uint32_t sb, int lane, const Q& qf, float (&s)[NTW][4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int rlo = 2 * gid + (tig >> 1), rhi = 2 * (gid + 8) + (tig >> 1);
+  // group scales of tokens gid and gid+8 (row 32: [16 tokens][4] fp16)
+  uint2 sl, sh;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(sl.x), "=r"(sl.y) : "r"(sb + swz128(32, 8 * gid)));
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(sh.x), "=r"(sh.y) : "r"(sb + swz128(32, 8 * (gid + 8))));
+  const float2 sl01 = __half22float2(*reinterpret_cast<const __half2*>(&sl.x));
+  const float2 sl23 = __half22float2(*reinterpret_cast<const __half2*>(&sl.y));
+  const float2 sh01 = __half22float2(*reinterpret_cast<const __half2*>(&sh.x));
+  const float2 sh23 = __half22float2(*reinterpret_cast<const __half2*>(&sh.y));
+  const float slo[4] = {sl01.x, sl01.y, sl23.x, sl23.y}, shi[4] = {sh01.x, sh01.y, sh23.x, sh23.y};
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // chunk 4*(tig & 1) + c: group c, k-steps 4c .. 4c+3
+    const uint4 klo = lds128(sb + swz128(rlo, 16 * (4 * (tig & 1) + c)));
+    const uint4 khi = lds128(sb + swz128(rhi, 16 * (4 * (tig & 1) + c)));
+    const uint32_t wl[4] = {klo.x, klo.y, klo.z, klo.w};
+    const uint32_t wh[4] = {khi.x, khi.y, khi.z, khi.w};
+    float acc[NTW][4];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int kk = 4 * c + q;
+      uint32_t af[4];
+      s8x4_to_f16x2x2(wl[q], af[0], af[2]);  // token gid: dims +0,+1 and +2,+3
+      s8x4_to_f16x2x2(wh[q], af[1], af[3]);  // token gid+8
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) {
+        const uint2 qv = qf.get(nt, kk);
+        mma_f16_16816(acc[nt], af, qv.x, qv.y);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+      s[nt][0] = fmaf(acc[nt][0], slo[c], s[nt][0]);
+      s[nt][1] = fmaf(acc[nt][1], slo[c], s[nt][1]);
+      s[nt][2] = fmaf(acc[nt][2], shi[c], s[nt][2]);
+      s[nt][3] = fmaf(acc[nt][3], shi[c], s[nt][3]);
+    }
+  }
+}
+
+// O^T += V^T P^T for one page: INT8 group-64 cache.  Pair row p (slots 2p,
+// 2p+1) holds 256 positions x 2 bytes at box rows 33 + 4p .. +3, position
+// 32*(d%8) + d/8 holding dim d, so lane (gid, tig) reads dims 8j + gid (j =
+// 0..31) of pairs tig and tig+4 as 64 contiguous bytes each: word w gives
+// m-tile w's rows gid (dim 16w + gid) and gid+8 (dim 16w + 8 + gid).  The
+// m-tiles of a 64-dim scale group share one scale per token, which scales
+// the P^T fragment (fp16) instead of the codes; tokens at or past page_lim
+// get a zero scale.
+template <int NTW>
+__device__ __forceinline__ void pv_int8(uint32_t sb, int lane, WarpState<NTW>& st,
+                                        const uint32_t (&pb)[NTW][2], int page_lim) {
+  const int gid = lane >> 2, tig = lane & 3;
+  // group scales of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 (row 65: [16][4] fp16)
+  auto ldsc = [&](int t) -> uint2 {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(sb + swz128(65, 8 * t)));
+    return v;
+  };
+  const uint2 s0 = ldsc(2 * tig), s1 = ldsc(2 * tig + 1), s2 = ldsc(2 * tig + 8), s3 = ldsc(2 * tig + 9);
+  auto keep = [&](int t) -> uint32_t {
+    return (t < page_lim ? 0x0000FFFFu : 0u) | (t + 1 < page_lim ? 0xFFFF0000u : 0u);
+  };
+  const uint32_t ma = keep(2 * tig), mb = keep(2 * tig + 8);
+  uint32_t pg[4][NTW][2];  // P^T fragments scaled by group g's token scales
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+    const uint32_t sa = prmt(g < 2 ? s0.x : s0.y, g < 2 ? s1.x : s1.y, sel) & ma;
+    const uint32_t sbb = prmt(g < 2 ? s2.x : s2.y, g < 2 ? s3.x : s3.y, sel) & mb;
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+      pg[g][nt][0] = hmul2(pb[nt][0], sa);
+      pg[g][nt][1] = hmul2(pb[nt][1], sbb);
+    }
+  }
+  const int rbase = 33 + (gid >> 1);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // chunk c: words 4c .. 4c+3 -> m-tiles 4c .. 4c+3 = group c
+    const uint4 va = lds128(sb + swz128(rbase + 4 * tig, 16 * (4 * (gid & 1) + c)));
+    const uint4 vb = lds128(sb + swz128(rbase + 4 * (tig + 4), 16 * (4 * (gid & 1) + c)));
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int mt = 4 * c + q;
+      uint32_t af[4];
+      s8x4_to_f16x2x2(wa[q], af[0], af[1]);  // pair tig: rows gid, gid+8
+      s8x4_to_f16x2x2(wb[q], af[2], af[3]);  // pair tig+4
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(st.o[mt][nt], af, pg[c][nt][0], pg[c][nt][1]);
+    }
+  }
+}
+
 // O^T += V^T P^T for one page: bf16 cache (V widened to fp16).
 template <int NTW>
 __device__ __forceinline__ void pv_bf16(uint32_t sb, int lane, WarpState<NTW>& st,
@@ -924,6 +1047,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int pg = 0; pg < NP; ++pg) {
         if constexpr (KVDT == PNKV_KV_NVFP4) qk_nvfp4<NTW>(sb[pg], lane, qf, sacc[pg]);
         else if constexpr (KVDT == PNKV_KV_FP8) qk_fp8<NTW>(sb[pg], lane, qf, sacc[pg]);
+        else if constexpr (KVDT == PNKV_KV_INT8) qk_int8<NTW>(sb[pg], lane, qf, sacc[pg]);
         else qk_bf16<NTW>(sb[pg], lane, qf, sacc[pg]);
       }
       softmax_pages<NTW, NP>(st, sacc, a.qk_scale_log2, key0, page_lim, masked, lane, pb);
@@ -931,6 +1055,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int pg = 0; pg < NP; ++pg) {
         if constexpr (KVDT == PNKV_KV_NVFP4) pv_nvfp4<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
         else if constexpr (KVDT == PNKV_KV_FP8) pv_fp8<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
+        else if constexpr (KVDT == PNKV_KV_INT8) pv_int8<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
         else pv_bf16<NTW>(sb[pg], lane, st, pb[pg], page_lim[pg]);
       }
       __syncwarp();
@@ -986,7 +1111,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
               int d;
               float2 v;
               const float w = wgt[nt][c];
-              if (KVDT != PNKV_KV_BF16) {
+              if constexpr (KVDT == PNKV_KV_INT8) {
+                // m-tile j: rows gid -> dim 16j + gid, rows gid+8 -> 16j + 8 + gid
+                mbuf[merge_pos(row, 16 * j + gid)] =
+                    (k == 0 ? 0.f : mbuf[merge_pos(row, 16 * j + gid)]) + st.o[j][nt][c] * w;
+                mbuf[merge_pos(row, 16 * j + 8 + gid)] =
+                    (k == 0 ? 0.f : mbuf[merge_pos(row, 16 * j + 8 + gid)]) + st.o[j][nt][c + 2] * w;
+                continue;
+              } else if (KVDT != PNKV_KV_BF16) {
                 const int mt = j & ~1;
                 const int e = (j & 1) ? c + 2 : c;
                 d = ((j & 1) ? 128 : 0) + 16 * gid + mt;
@@ -1153,9 +1285,10 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   a.num_pages = cache->num_pages;
   a.hkv = cache->num_kv_heads;
   a.group = group;
-  const float kscale = cache->dtype != PNKV_KV_BF16 ? cache->k_scale : 1.0f;
+  const bool tensor_scaled = cache->dtype == PNKV_KV_NVFP4 || cache->dtype == PNKV_KV_FP8;
+  const float kscale = tensor_scaled ? cache->k_scale : 1.0f;
   a.qk_scale_log2 = sm_scale * kscale * kLog2e;
-  a.out_scale = cache->dtype != PNKV_KV_BF16 ? cache->v_scale : 1.0f;
+  a.out_scale = tensor_scaled ? cache->v_scale : 1.0f;
   a.q = q_roped;
   a.qo_indptr = qo_indptr;
   a.page_table = page_table;
@@ -1175,10 +1308,12 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   CUtensorMap map;
   const int box_rows = cache->dtype == PNKV_KV_NVFP4 ? Geometry<PNKV_KV_NVFP4>::kBoxRows
                        : cache->dtype == PNKV_KV_FP8 ? Geometry<PNKV_KV_FP8>::kBoxRows
+                       : cache->dtype == PNKV_KV_INT8 ? Geometry<PNKV_KV_INT8>::kBoxRows
                                                      : Geometry<PNKV_KV_BF16>::kBoxRows;
   if ((st = make_pool_map(cache, box_rows, &map)) != PNKV_OK) return st;
   cudaStream_t s = as_stream(stream);
   if (cache->dtype == PNKV_KV_NVFP4) return dispatch_rows<PNKV_KV_NVFP4>(map, a, grid, s);
   if (cache->dtype == PNKV_KV_FP8) return dispatch_rows<PNKV_KV_FP8>(map, a, grid, s);
+  if (cache->dtype == PNKV_KV_INT8) return dispatch_rows<PNKV_KV_INT8>(map, a, grid, s);
   return dispatch_rows<PNKV_KV_BF16>(map, a, grid, s);
 }

@@ -140,6 +140,18 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
       : "r"(w));
 }
 
+// Four int8 as two fp16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi), exactly: a
+// byte b biased to u = b ^ 0x80 becomes the fp16 1024 + u (its bits 0x6400 |
+// u), and subtracting 1152 leaves the signed value.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(t), "r"(0x64646464u), "r"(0x5150u));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b) : "r"(t), "r"(0x64646464u), "r"(0x5352u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
 // fp32 -> E4M3 byte, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float x) {
   uint16_t out;

@@ -55,10 +55,11 @@ inline int check_cache(const pnkv_cache* c) {
   if (!c || !c->pool || c->num_pages <= 0 || c->page_size != 16 || c->head_dim != 256 ||
       c->num_kv_heads < 1 || c->num_kv_heads > 16)
     return PNKV_ERR_INVALID_ARG;
-  if (c->dtype != PNKV_KV_BF16 && c->dtype != PNKV_KV_NVFP4 && c->dtype != PNKV_KV_FP8)
+  if (c->dtype != PNKV_KV_BF16 && c->dtype != PNKV_KV_NVFP4 && c->dtype != PNKV_KV_FP8 &&
+      c->dtype != PNKV_KV_INT8)
     return PNKV_ERR_INVALID_ARG;
   if (!aligned(c->pool, 128)) return PNKV_ERR_INVALID_ARG;
-  if (c->dtype != PNKV_KV_BF16) {
+  if (c->dtype == PNKV_KV_NVFP4 || c->dtype == PNKV_KV_FP8) {
     if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || !std::isfinite(c->k_scale) ||
         !std::isfinite(c->v_scale))
       return PNKV_ERR_INVALID_ARG;
@@ -70,6 +71,7 @@ inline int check_cache(const pnkv_cache* c) {
 inline int64_t head_record_bytes(int dtype) {
   if (dtype == PNKV_KV_NVFP4) return 2 * 16 * (128 + 16);
   if (dtype == PNKV_KV_FP8) return 2 * 16 * 256;
+  if (dtype == PNKV_KV_INT8) return 2 * 16 * (256 + 8);
   return 2 * 16 * 256 * 2;
 }
 

@@ -1,5 +1,5 @@
 // kv_append_nvfp4: fused rope + quantise + page scatter for the step's new
-// tokens (NVFP4, FP8 or bf16 pools).
+// tokens (NVFP4, FP8, INT8 group-64 or bf16 pools).
 //
 // Rope with the YaRN table, mscale already inside cos/sin ("A 1,048,576-token
 // context on two RTX 5090s", section "YaRN, and matching what vLLM actually
@@ -12,7 +12,10 @@
 // cache of the comparison engine in "A 1,048,576-token context on two RTX
 // 5090s", section "Against vLLM: prefill loses, decode wins, and one
 // surprise") stores E4M3(x * fp32(1/g)) per element with one scale g per
-// tensor.
+// tensor.  An INT8 pool (the TP2 README's million-token cache, sections
+// "Dual-GPU (TP2) and YaRN 1M context" and "Memory, per GPU": INT8 with one
+// scale per 64 elements) stores s = fp16_rn_satfinite(fp32(a / 127)) per
+// 64-element group and codes RNE(fp32(x * fp32(1/s))) clamped to +-127.
 //
 // One warp per (token, head) row of 256 elements: lane l owns elements
 // 8l .. 8l+7 (one 16-byte load).  Rope partners (j, j + R/2) sit R/16 lanes
@@ -68,6 +71,36 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
 // conversion does with the sign of a zero result).
 __device__ __forceinline__ uint32_t e4m3_code(float y) {
   return (f32_to_e4m3_satfinite(y) & 0xFFu) | ((__float_as_uint(y) >> 31) << 7);
+}
+
+// INT8 group-64: this lane's 8 elements are part of the group of lanes
+// 8m .. 8m+7.  Returns the 8 codes (two words, element i in byte i % 4 of
+// word i / 4); *scale gets the group's fp16 scale bits.
+__device__ __forceinline__ uint2 quantize8_int8(const float (&x)[8], uint32_t* scale) {
+  float a = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+  // satfinite: values past the largest fp16 clamp to it before the rounding
+  const __half s16 = __float2half_rn(fminf(__fdiv_rn(a, 127.0f), 65504.0f));
+  const float d = __half2float(s16);
+  uint2 out = make_uint2(0, 0);
+  if (d != 0.f) {
+    const float r = __frcp_rn(d);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int q = max(-127, min(127, __float2int_rn(__fmul_rn(x[e], r))));
+      const uint32_t b = static_cast<uint32_t>(q) & 0xFFu;
+      if (e < 4) out.x |= b << (8 * e);
+      else out.y |= b << (8 * (e - 4));
+    }
+    *scale = __half_as_ushort(s16);
+  } else {
+    *scale = 0;
+  }
+  return out;
 }
 
 // Quantise this lane's 8 elements (part of the 16-element block shared with
@@ -196,6 +229,24 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
     if (a.dtype == PNKV_KV_BF16) {
       reinterpret_cast<uint4*>(rec + slot * 512)[lane] = pack_bf16x8(kx);
       reinterpret_cast<uint4*>(rec + 8192 + slot * 512)[lane] = vraw;
+    } else if (a.dtype == PNKV_KV_INT8) {
+      // K codes [16][256]: dim 8*lane + i at 64*(2*(lane & 1) + i/4) +
+      // 4*(lane/2) + i%4 of the slot's row (two 4-byte runs); V codes
+      // [8 pairs][256 positions][2]: dim 8*lane + i at position 32*i + lane;
+      // scales [16][4] fp16 after each
+      uint32_t ks, vs;
+      const uint2 kc = quantize8_int8(kx, &ks);
+      const uint2 vc = quantize8_int8(vx, &vs);
+      const int p0 = 128 * (lane & 1) + 4 * (lane >> 1);
+      *reinterpret_cast<uint32_t*>(rec + slot * 256 + p0) = kc.x;
+      *reinterpret_cast<uint32_t*>(rec + slot * 256 + p0 + 64) = kc.y;
+      uint8_t* vrow = rec + 4224 + (slot >> 1) * 512 + 2 * lane + (slot & 1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vrow[64 * i] = static_cast<uint8_t>(((i < 4 ? vc.x : vc.y) >> (8 * (i & 3))) & 0xFFu);
+      if ((lane & 7) == 0) {
+        reinterpret_cast<uint16_t*>(rec + 4096 + slot * 8)[lane >> 3] = static_cast<uint16_t>(ks);
+        reinterpret_cast<uint16_t*>(rec + 8320 + slot * 8)[lane >> 3] = static_cast<uint16_t>(vs);
+      }
     } else if (a.dtype == PNKV_KV_FP8) {
       // K codes [16][256]: bytes 8*lane .. +7 of the slot's row; V codes
       // [8 pairs][256][2]: byte 2d + (slot odd) of the pair's row
@@ -245,7 +296,7 @@ extern "C" int kv_append_nvfp4(const pnkv_cache* cache, const int32_t* page_tabl
   using namespace pnkv;
   int st = check_cache(cache);
   if (st != PNKV_OK) return st;
-  if (cache->dtype != PNKV_KV_BF16) {
+  if (cache->dtype == PNKV_KV_NVFP4 || cache->dtype == PNKV_KV_FP8) {
     // keep d = E4M3(S) * g (NVFP4), 1/g (FP8) and 1/d normal binary32 numbers
     const float lo = 7.8886091e-31f, hi = 1.2676506e30f;  // 2^-100, 2^100
     if (cache->k_scale < lo || cache->k_scale > hi || cache->v_scale < lo || cache->v_scale > hi)

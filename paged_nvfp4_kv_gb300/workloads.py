@@ -51,7 +51,7 @@ class Workload:
     positions that the step appends and attends with."""
     name: str
     seed: int
-    kv_dtype: str                     # "nvfp4", "fp8" or "bf16"
+    kv_dtype: str                     # "nvfp4", "fp8", "int8" or "bf16"
     cached: np.ndarray                # [B] int64
     qlen: np.ndarray                  # [B] int64
     num_q_heads: int = HQ
@@ -229,6 +229,11 @@ def million_token_decode_fp8(seed=1003):
     return build("million-token decode (1,048,576 FP8 keys)", seed, "fp8", [1048575], [1])
 
 
+def million_token_decode_int8(seed=1003):
+    """The million-token decode with an INT8 group-64 cache."""
+    return build("million-token decode (1,048,576 INT8 group-64 keys)", seed, "int8", [1048575], [1])
+
+
 CONFIGS = {1: tiny_decode, 2: native_window_decode, 3: million_token_decode,
            4: multi_session_verify, 5: chunked_prefill, 6: chunked_prefill_reduced,
-           7: million_token_decode_fp8}
+           7: million_token_decode_fp8, 8: million_token_decode_int8}

@@ -27,7 +27,7 @@ def roped_new_q(w, cos_t, sin_t):
 def pool(w, cos_t, sin_t, sequences=None, chunk=65536):
     """The pool after the cache fill and the step's append, built by the
     oracle: K roped with the given tables, then encoded into its pages."""
-    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "bf16": OP.BF16}[w.kv_dtype]
+    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "int8": OP.INT8, "bf16": OP.BF16}[w.kv_dtype]
     P = OP.new_pool(w.num_pages, dtype, w.num_kv_heads, w.head_dim)
     R = w.yarn["rotary_dim"]
     for b in (range(w.batch) if sequences is None else sequences):
@@ -45,7 +45,7 @@ def pool(w, cos_t, sin_t, sequences=None, chunk=65536):
 def pool_pages(w, cos_t, sin_t, b, positions):
     """Oracle bytes of the pages holding ``positions`` of sequence b (used for
     sampled checks at full size).  Returns {page id: bytes}."""
-    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "bf16": OP.BF16}[w.kv_dtype]
+    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "int8": OP.INT8, "bf16": OP.BF16}[w.kv_dtype]
     R = w.yarn["rotary_dim"]
     pages = sorted(set(int(p) // 16 for p in positions))
     out = {}
@@ -64,7 +64,7 @@ def pool_pages(w, cos_t, sin_t, b, positions):
 
 def attention(w, pool_bytes, q_roped, rows=None):
     """{(token, head): (o [D], lse)} over the given pool bytes."""
-    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "bf16": OP.BF16}[w.kv_dtype]
+    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "int8": OP.INT8, "bf16": OP.BF16}[w.kv_dtype]
     return OA.paged_decode(pool_bytes, dtype, w.num_kv_heads, w.head_dim, q_roped, w.qo_indptr,
                            w.page_table, w.seq_lens, w.num_q_heads, w.causal, w.g_k, w.g_v,
                            rows=rows)

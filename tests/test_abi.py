@@ -81,6 +81,8 @@ def test_page_bytes(lib):
     assert lib.pnkv_page_bytes(ctypes.byref(_cache(dtype=2)), ctypes.byref(out)) == 0
     assert out.value == 32768
     assert lib.pnkv_page_bytes(ctypes.byref(_cache(dtype=2, k_scale=-1.0)), ctypes.byref(out)) == -1
+    assert lib.pnkv_page_bytes(ctypes.byref(_cache(dtype=3, k_scale=0.0)), ctypes.byref(out)) == 0
+    assert out.value == 33792
     for bad in (dict(page_size=32), dict(head_dim=128), dict(dtype=5), dict(pool=None),
                 dict(pool=1000), dict(k_scale=0.0), dict(v_scale=float("inf")), dict(num_pages=0),
                 dict(num_kv_heads=0)):

@@ -102,6 +102,15 @@ def test_million_token_decode_fp8_full():
     _check(w, s, o32, o16, rows, {0: _pages_of(w, 0, np.random.default_rng(7))})
 
 
+def test_million_token_decode_int8_full():
+    """The million-token decode with an INT8 group-64 pool."""
+    from paged_nvfp4_kv_gb300 import workloads as W
+    w = W.million_token_decode_int8()
+    s, o32, o16 = _run(w)
+    rows = [(0, h) for h in (1, 12, 22)]
+    _check(w, s, o32, o16, rows, {0: _pages_of(w, 0, np.random.default_rng(8))})
+
+
 def test_multi_session_verify_full():
     from paged_nvfp4_kv_gb300 import workloads as W
     w = W.multi_session_verify()

@@ -70,6 +70,12 @@ CASES = {
     "qlen8-fp8": ("fp8", [300, 1800], [8, 3]),
     "page-edge-fp8": ("fp8", [16, 15, 17, 31, 32, 0], [1, 1, 1, 1, 1, 1]),
     "long-fp8": ("fp8", [70000, 7000], [1, 1]),
+    # INT8 group-64 pools
+    "ragged-int8": ("int8", [1000, 36, 4100], [1, 1, 1]),
+    "verify5-int8": ("int8", [700, 50, 333, 2011], [5, 5, 5, 5]),
+    "qlen8-int8": ("int8", [300, 1800], [8, 3]),
+    "page-edge-int8": ("int8", [16, 15, 17, 31, 32, 0], [1, 1, 1, 1, 1, 1]),
+    "long-int8": ("int8", [70000, 7000], [1, 1]),
     # more than 64 query rows per KV head: the tensor-core tile path
     "prefill-nvfp4": ("nvfp4", [3000, 500, 77], [100, 37, 1]),
     "prefill-long-nvfp4": ("nvfp4", [40000], [300]),
@@ -156,12 +162,12 @@ def test_page_permutation_invariance():
     assert torch.equal(again.view(torch.int32), out32.view(torch.int32))
 
 
-def test_fp8_prefill_chunk_is_unsupported():
+@pytest.mark.parametrize("dtype", ["fp8", "int8", "bf16"])
+def test_prefill_chunk_needs_nvfp4(dtype):
     """More than 64 query rows per KV head run the tensor-core tile, built for
-    NVFP4 pools only: an FP8 pool gets PNKV_ERR_UNSUPPORTED, nothing runs."""
-    from paged_nvfp4_kv_gb300 import _lib
+    NVFP4 pools only: other pools get PNKV_ERR_UNSUPPORTED, nothing runs."""
     from paged_nvfp4_kv_gb300.engine import DecodeSession
-    w = _workload("fp8-chunk", "fp8", [500], [20])
+    w = _workload("chunk-" + dtype, dtype, [500], [20])
     s = DecodeSession(w)
     s.fill()
     s.append()

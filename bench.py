@@ -219,6 +219,14 @@ def cpu_info():
     return cores
 
 
+def workload_config(w, world):
+    """The ``config`` object of both arms' JSON lines."""
+    return {"workload": w.name, "keys": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype,
+            "query_rows": int(w.total_q) * w.num_q_heads, "heads": "24q/4kv x 256",
+            "pages": int(w.num_pages), "l2": "inputs larger than L2 (no flush)",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -239,7 +247,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "keys": int(w.seq_lens.sum()), "kv_dtype": w.kv_dtype},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d of %d keys of sequence 0, all %d query heads, per step"
                                    % (keys, int(w.seq_lens[0]), w.num_q_heads)},
@@ -374,10 +382,7 @@ def run_ours(args):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16-mma/fp32-softmax over %s KV" % w.kv_dtype,
         "data": "synthetic",
-        "config": {"workload": w.name, "keys": keys, "kv_dtype": w.kv_dtype,
-                   "query_rows": int(w.total_q) * w.num_q_heads, "heads": "24q/4kv x 256",
-                   "pages": int(w.num_pages), "l2": "inputs larger than L2 (no flush)",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": workload_config(w, world),
         "kernels_ms": {"kv_append_nvfp4": append_ms, "paged_decode_attention": decode_ms,
                        "split_kv_combine": combine_ms},
         "hbm_gbs_decode": achieved,

@@ -173,44 +173,61 @@ def workload(cfg):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 
-def oracle_rate(w, seconds, max_keys=None):
-    """KV tokens/s/layer of the float64 oracle on the host cores: rope and
-    encode the sampled keys (untimed), then time the oracle's paged
-    attention of all query rows of sequence 0 over a sample of its keys,
-    sized to take about ``seconds``."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import oracle_path
-    from oracle import attention as OA
-    from oracle import paged as OP
-    from oracle import yarn as OY
+class OracleSampler:
+    """The float64 oracle's paged attention on the host cores, over a sample
+    of sequence 0's last n keys: the rope table, the roped keys and the
+    encoded pool are built once (untimed); ``time()`` runs the attention of
+    all of the sequence's query rows over the sample once."""
 
-    L = int(w.seq_lens[0])
-    dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "int8": OP.INT8, "bf16": OP.BF16}[w.kv_dtype]
-    R = w.yarn["rotary_dim"]
+    def __init__(self, w):
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        import oracle_path
+        from oracle import attention as OA
+        from oracle import paged as OP
+        from oracle import yarn as OY
+        self.w, self.OA, self.OP = w, OA, OP
+        self.L = int(w.seq_lens[0])
+        self.dtype = {"nvfp4": OP.NVFP4, "fp8": OP.FP8, "int8": OP.INT8, "bf16": OP.BF16}[w.kv_dtype]
+        self.cos_t, self.sin_t = OY.rope_tables(w.yarn, self.L)
+        self.q = oracle_path.roped_new_q(w, self.cos_t, self.sin_t)[: int(w.qlen[0])]
+        self.OY = OY
+        self.n = 0
 
-    def run(n):
-        cos_t, sin_t = OY.rope_tables(w.yarn, L)
+    def prepare(self, n):
+        w, OP = self.w, self.OP
+        n = max(16, min(self.L, (n // 16) * 16))
         npg = (n + 15) // 16
-        pool = OP.new_pool(npg, dtype, w.num_kv_heads, w.head_dim)
-        table = np.arange(npg, dtype=np.int32)
-        k = w.k_rows(0, L - n, L).astype(np.float64)
-        v = w.v_rows(0, L - n, L).astype(np.float64)
-        kr = OY.rope_rows(k, np.arange(L - n, L), cos_t, sin_t, R)
-        OP.scatter_sequence_fast(pool, dtype, w.num_kv_heads, w.head_dim, table, 0, kr, v, w.g_k,
-                                 w.g_v)
-        q = oracle_path.roped_new_q(w, cos_t, sin_t)[: int(w.qlen[0])]
+        self.pool = OP.new_pool(npg, self.dtype, w.num_kv_heads, w.head_dim)
+        self.table = np.arange(npg, dtype=np.int32)
+        k = w.k_rows(0, self.L - n, self.L).astype(np.float64)
+        v = w.v_rows(0, self.L - n, self.L).astype(np.float64)
+        kr = self.OY.rope_rows(k, np.arange(self.L - n, self.L), self.cos_t, self.sin_t, w.yarn["rotary_dim"])
+        OP.scatter_sequence_fast(self.pool, self.dtype, w.num_kv_heads, w.head_dim, self.table, 0, kr, v,
+                                 w.g_k, w.g_v)
+        self.n = n
+        return n
+
+    def time(self):
+        w = self.w
         t0 = time.perf_counter()
-        OA.paged_decode(pool, dtype, w.num_kv_heads, w.head_dim, q, np.array([0, q.shape[0]]),
-                        table[None, :], np.array([n]), w.num_q_heads, True, w.g_k, w.g_v)
+        self.OA.paged_decode(self.pool, self.dtype, w.num_kv_heads, w.head_dim, self.q,
+                             np.array([0, self.q.shape[0]]), self.table[None, :], np.array([self.n]),
+                             w.num_q_heads, True, w.g_k, w.g_v)
         return time.perf_counter() - t0
 
-    n = min(L, 16384)
-    dt = run(n)
-    target = max(n, min(L if max_keys is None else max_keys, int(n * seconds / max(dt, 1e-3))))
-    target = (target // 16) * 16 or 16
-    if target > n:
-        n = target
-        dt = run(n)
+    def calibrate(self, seconds, n0=4096):
+        """Prepare a sample that takes about ``seconds`` per ``time()``."""
+        self.prepare(n0)
+        dt = self.time()
+        return self.prepare(int(self.n * seconds / max(dt, 1e-4)))
+
+
+def oracle_rate(w, seconds):
+    """KV tokens/s/layer of the float64 oracle over a sample of sequence 0's
+    keys sized to take about ``seconds``."""
+    o = OracleSampler(w)
+    n = o.calibrate(seconds)
+    dt = o.time()
     return n / dt, n, dt
 
 
@@ -232,12 +249,14 @@ def run_reference(args):
     if rank != 0:
         return
     w = workload(args.config)
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    # each step is one oracle pass over a bounded sample, sized so the whole
+    # run takes about two minutes of host time
+    per_step = min(2.0, max(0.01, 120.0 / max(1, args.steps + args.warmup)))
+    o = OracleSampler(w)
+    keys = o.calibrate(per_step)
     times = []
-    keys = None
     for i in range(args.warmup + args.steps):
-        rate, n, dt = oracle_rate(w, per_step)
-        keys = n
+        dt = o.time()
         if i >= args.warmup:
             times.append(dt)
     rate = keys / float(np.mean(times))

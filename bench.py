@@ -49,6 +49,23 @@ def parse():
     return p.parse_args()
 
 
+def replica_max(x, world, device):
+    """Max of ``x`` over the ranks (the slowest replica sets the time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(units_per_rank, ms, world):
+    """Whole-job rate: the units all ranks processed over the max-over-ranks
+    time (replicas each process the same workload)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -333,17 +350,15 @@ def run_ours(args):
                              w_.num_q_heads, w_.num_kv_heads, s.max_qlen, s.out, s.lse, stream)
             ev[i][3].record(stream)
     stream.synchronize()
-    total_ms = start.elapsed_time(stop)
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        dist.barrier()
+    total_ms = replica_max(start.elapsed_time(stop), world, "cuda")
     append_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
     combine_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
     ms_per_step = total_ms / K
     keys = int(w.seq_lens.sum())
-    value = world * keys / (ms_per_step * 1e-3)
+    value = replica_rate(keys, ms_per_step, world)
     err = s.error_word()
 
     # ---- end to end through the public API, host buffers
@@ -372,12 +387,8 @@ def run_ours(args):
             out_h.copy_(s.out, non_blocking=True)
         e1.record(stream)
         stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * keys / (e2e_ms * 1e-3)
+    e2e_ms = replica_max(e0.elapsed_time(e1) / K, world, "cuda")
+    e2e_value = replica_rate(keys, e2e_ms, world)
 
     peak, peak_kind = peaks()
     algo_bytes = keys * ALGO_BYTES_PER_TOKEN[w.kv_dtype]

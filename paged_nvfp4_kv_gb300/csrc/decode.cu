@@ -45,6 +45,7 @@ int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32
                    int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal, float* o_part,
                    float* lse_part, int64_t part_slots, int32_t* work_meta, int32_t* dev_err,
                    cudaStream_t stream);
+int prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t max_qlen, int sms);
 
 namespace {
 
@@ -1240,12 +1241,14 @@ extern "C" int64_t pnkv_decode_slots(const pnkv_cache* cache, int32_t batch, int
   if (st != PNKV_OK) return st;
   if (batch < 1 || max_qlen < 1 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
     return PNKV_ERR_INVALID_ARG;
-  // the tensor-core tile path (more than 64 rows per KV head) writes one slot
-  // per (sequence, KV head); the split-KV path one per piece
-  if (static_cast<int64_t>(num_q_heads / cache->num_kv_heads) * max_qlen > 64)
-    return static_cast<int64_t>(batch) * cache->num_kv_heads;
   int grid = 0;
   if ((st = decode_grid(&grid)) != PNKV_OK) return st;
+  // the tensor-core tile path (more than 64 rows per KV head) writes one slot
+  // per (sequence, KV head, key split); the split-KV path one per piece
+  const int32_t group = num_q_heads / cache->num_kv_heads;
+  if (static_cast<int64_t>(group) * max_qlen > 64)
+    return static_cast<int64_t>(batch) * cache->num_kv_heads *
+           prefill_splits(batch, cache->num_kv_heads, group, max_qlen, grid);
   return static_cast<int64_t>(batch) * cache->num_kv_heads + grid;
 }
 

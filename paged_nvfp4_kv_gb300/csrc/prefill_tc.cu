@@ -33,6 +33,7 @@
 // decode path.  The CTA writes one normalised partial (with its natural-log
 // LSE) per row into the (sequence, KV head) slot, which split_kv_combine
 // passes through.
+#include <algorithm>
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -117,6 +118,7 @@ struct PrefillArgs {
   int64_t pt_stride;
   const int32_t* seq_lens;
   int32_t batch, hq, max_qlen, rows_per_slot, causal;
+  int32_t splits;  // key-range splits per tile (slots per (sequence, KV head))
   float* o_part;
   float* lse_part;
   int64_t part_slots;
@@ -208,13 +210,17 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // --------------------------------------------------------------- tiles --
-// Tiles enumerate (sequence, KV head, token tile); every role of a CTA walks
-// the same list: tile = blockIdx.x + k * gridDim.x.
+// Work items enumerate (sequence, KV head, token tile, key split); every role
+// of a CTA walks the same list: item = blockIdx.x + k * gridDim.x.  When
+// there are too few token tiles to fill the GPU, each tile's key blocks are
+// cut into `splits` ranges whose partials split_kv_combine merges.
 struct Tile {
   int b, h;
   int t0, ntok;      // first query token (within the chunk) and tokens in tile
   int q0, qlen, len; // qo_indptr[b], chunk length, keys of the sequence
-  int nblocks;       // key blocks the tile needs
+  int split;         // key range of the item: blocks kb0 .. kb0 + nblocks - 1
+  int kb0;
+  int nblocks;
   int keys;          // keys the last row of the tile may see
 };
 
@@ -233,19 +239,24 @@ __device__ bool find_tile(const PrefillArgs& a, int64_t idx, Tile* t) {
     int q0, qlen, len;
     if (!seq_ok(a, b, &q0, &qlen, &len)) continue;
     const int per_head = (qlen + a.tpt - 1) / a.tpt;
-    const int64_t n = static_cast<int64_t>(per_head) * a.hkv;
+    const int64_t per_h = static_cast<int64_t>(per_head) * a.splits;
+    const int64_t n = per_h * a.hkv;
     if (idx < base + n) {
       const int64_t r = idx - base;
       t->b = b;
-      t->h = static_cast<int>(r / per_head);
-      const int tt = static_cast<int>(r % per_head);
+      t->h = static_cast<int>(r / per_h);
+      const int64_t rem = r % per_h;
+      const int tt = static_cast<int>(rem / a.splits);
+      t->split = static_cast<int>(rem % a.splits);
       t->t0 = tt * a.tpt;
       t->ntok = min(a.tpt, qlen - t->t0);
       t->q0 = q0;
       t->qlen = qlen;
       t->len = len;
       t->keys = a.causal ? len - qlen + t->t0 + t->ntok : len;
-      t->nblocks = (t->keys + kBlockKeys - 1) / kBlockKeys;
+      const int nb = (t->keys + kBlockKeys - 1) / kBlockKeys;
+      t->kb0 = static_cast<int>(static_cast<int64_t>(t->split) * nb / a.splits);
+      t->nblocks = static_cast<int>(static_cast<int64_t>(t->split + 1) * nb / a.splits) - t->kb0;
       return true;
     }
     base += n;
@@ -350,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t page = -1;
         bool in_seq = false;
         if (lane < kBlockPages) {
-          const int pi = kBlockPages * j + lane;
+          const int pi = kBlockPages * (t.kb0 + j) + lane;
           in_seq = pi < pages;
           if (in_seq) {
             page = __ldg(row + pi);
@@ -610,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the row maximum of the raw logits over the visible keys (masked
         // keys become -inf); the logit scale is positive, so the maximum of
         // the scaled logits is the scaled maximum
-        const int key0 = j * kBlockKeys;
+        const int key0 = (t.kb0 + j) * kBlockKeys;
         float mraw = -INFINITY;
         if (__all_sync(0xffffffffu, key0 + kBlockKeys <= lim)) {
 #pragma unroll
@@ -680,16 +691,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       gb = g0 + t.nblocks;
-      // epilogue: final O row, normalised, into the (sequence, KV head) slot
-      const int64_t gl = gb - 1;
-      ok = wait_warp(B_PV_DONE + static_cast<int>(gl % kPStages), ring_parity(gl, kPStages));
-      if (!ok) break;
-      tc_fence_after();
+      // epilogue: final O row, normalised, into the (sequence, KV head,
+      // split) slot (an item with no key block writes zeros and LSE -inf)
+      if (t.nblocks > 0) {
+        const int64_t gl = gb - 1;
+        ok = wait_warp(B_PV_DONE + static_cast<int>(gl % kPStages), ring_parity(gl, kPStages));
+        if (!ok) break;
+        tc_fence_after();
+      }
       const int64_t seg = static_cast<int64_t>(t.b) * a.hkv + t.h;
+      const int64_t slot = seg * a.splits + t.split;
       const int64_t n = static_cast<int64_t>(tok) * a.group + head;
-      const float inv = l > 0.f ? a.out_scale / l : 0.f;
-      float* dst = a.o_part + (seg * a.rows_per_slot + n) * 256;
-      const bool write = row_live && seg < a.part_slots && n < a.rows_per_slot;
+      const bool have = l > 0.f;
+      const float inv = have ? a.out_scale / l : 0.f;
+      float* dst = a.o_part + (slot * a.rows_per_slot + n) * 256;
+      const bool write = row_live && slot < a.part_slots && n < a.rows_per_slot;
 #pragma unroll 1
       for (int c = 0; c < 256; c += 16) {
         uint32_t x[16];
@@ -699,15 +715,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
             *reinterpret_cast<float4*>(dst + c + e) =
-                make_float4(__uint_as_float(x[e]) * inv, __uint_as_float(x[e + 1]) * inv,
-                            __uint_as_float(x[e + 2]) * inv, __uint_as_float(x[e + 3]) * inv);
+                have ? make_float4(__uint_as_float(x[e]) * inv, __uint_as_float(x[e + 1]) * inv,
+                                   __uint_as_float(x[e + 2]) * inv, __uint_as_float(x[e + 3]) * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       tc_fence_before();
-      if (write) a.lse_part[seg * a.rows_per_slot + n] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-      if (r == 0 && t.t0 == 0) {
-        a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg);
-        a.work_meta[4 + 2 * seg + 1] = 1;
+      if (write) a.lse_part[slot * a.rows_per_slot + n] = have ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (r == 0 && t.t0 == 0 && t.split == 0) {
+        a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg * a.splits);
+        a.work_meta[4 + 2 * seg + 1] = a.splits;
       }
     }
   }
@@ -744,6 +761,18 @@ __global__ void prefill_meta_kernel(const PrefillArgs a) {
 
 }  // namespace
 
+// Key-range splits per tile: 1 when there are at least four token tiles per SM
+// (the chunked-prefill workload: 1,564 tiles), else enough splits (at most 8)
+// to give every SM about four work items.  Host only; the tile count used is
+// the bound batch * KV heads * ceil(max_qlen / tokens per tile).
+int prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t max_qlen, int sms) {
+  const int tpt = 128 / group;
+  const int64_t tiles = static_cast<int64_t>(batch) * num_kv_heads * ((max_qlen + tpt - 1) / tpt);
+  const int64_t want = 4 * static_cast<int64_t>(sms);
+  if (tiles >= want) return 1;
+  return static_cast<int>(std::min<int64_t>(8, (want + tiles - 1) / tiles));
+}
+
 // Launch the tensor-core tile path (called by paged_decode_attention when a KV
 // head has more than 64 query rows).
 int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32_t* qo_indptr,
@@ -774,12 +803,13 @@ int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32
   a.part_slots = part_slots;
   a.work_meta = work_meta;
   a.dev_err = dev_err;
-  if (part_slots < static_cast<int64_t>(batch) * a.hkv) return PNKV_ERR_INVALID_ARG;
   CUtensorMap map;
   int st = make_pool_map(cache, 36, &map);
   if (st != PNKV_OK) return st;
   int sms = 0;
   if ((st = device_sm_count(&sms)) != PNKV_OK) return st;
+  a.splits = prefill_splits(batch, a.hkv, a.group, max_qlen, sms);
+  if (part_slots < static_cast<int64_t>(batch) * a.hkv * a.splits) return PNKV_ERR_INVALID_ARG;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(prefill_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=

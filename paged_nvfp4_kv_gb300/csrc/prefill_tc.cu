@@ -761,16 +761,26 @@ __global__ void prefill_meta_kernel(const PrefillArgs a) {
 
 }  // namespace
 
-// Key-range splits per tile: 1 when there are at least four token tiles per SM
-// (the chunked-prefill workload: 1,564 tiles), else enough splits (at most 8)
-// to give every SM about four work items.  Host only; the tile count used is
-// the bound batch * KV heads * ceil(max_qlen / tokens per tile).
+// Key-range splits per tile, chosen so that the work items fill the SMs'
+// last wave: with T tiles and S SMs, s splits make T*s items in ceil(T*s/S)
+// waves, a fraction (T*s/S) / ceil(T*s/S) of the GPU busy.  The smallest s
+// (at most 8) within 1 % of the best fraction wins.  Host only; T is the
+// bound batch * KV heads * ceil(max_qlen / tokens per tile).
 int prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t max_qlen, int sms) {
   const int tpt = 128 / group;
   const int64_t tiles = static_cast<int64_t>(batch) * num_kv_heads * ((max_qlen + tpt - 1) / tpt);
-  const int64_t want = 4 * static_cast<int64_t>(sms);
-  if (tiles >= want) return 1;
-  return static_cast<int>(std::min<int64_t>(8, (want + tiles - 1) / tiles));
+  if (tiles <= 0 || sms <= 0) return 1;
+  double busy[9] = {0.0};
+  double best = 0.0;
+  for (int s = 1; s <= 8; ++s) {
+    const int64_t items = tiles * s;
+    const int64_t waves = (items + sms - 1) / sms;
+    busy[s] = static_cast<double>(items) / static_cast<double>(waves * sms);
+    best = std::max(best, busy[s]);
+  }
+  for (int s = 1; s <= 8; ++s)
+    if (busy[s] >= best - 0.01) return s;
+  return 1;
 }
 
 // Launch the tensor-core tile path (called by paged_decode_attention when a KV

@@ -1103,39 +1103,39 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int row = row_base + 8 * nt + 2 * tig + c;
-#pragma unroll
             // pairs of adjacent dims: bf16 m-tile mt holds dims 32*gid + 2*mt
-            // (c) and +1 (c + 2); NVFP4 m-tiles mt, mt+1 hold dims 16*gid + mt,
-            // +1 (c) and 128 + 16*gid + mt, +1 (c + 2)
+            // (c) and +1 (c + 2); NVFP4/FP8 m-tiles mt, mt+1 hold dims
+            // 16*gid + mt, +1 (c) and 128 + 16*gid + mt, +1 (c + 2); INT8
+            // m-tile mt holds dims 16*mt + gid (c) and 16*mt + 8 + gid (c + 2)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              int d;
-              float2 v;
               const float w = wgt[nt][c];
               if constexpr (KVDT == PNKV_KV_INT8) {
-                // m-tile j: rows gid -> dim 16j + gid, rows gid+8 -> 16j + 8 + gid
-                mbuf[merge_pos(row, 16 * j + gid)] =
-                    (k == 0 ? 0.f : mbuf[merge_pos(row, 16 * j + gid)]) + st.o[j][nt][c] * w;
-                mbuf[merge_pos(row, 16 * j + 8 + gid)] =
-                    (k == 0 ? 0.f : mbuf[merge_pos(row, 16 * j + 8 + gid)]) + st.o[j][nt][c + 2] * w;
-                continue;
-              } else if (KVDT != PNKV_KV_BF16) {
-                const int mt = j & ~1;
-                const int e = (j & 1) ? c + 2 : c;
-                d = ((j & 1) ? 128 : 0) + 16 * gid + mt;
-                v = make_float2(st.o[mt][nt][e] * w, st.o[mt + 1][nt][e] * w);
+                float* d0 = mbuf + merge_pos(row, 16 * j + gid);
+                float* d1 = mbuf + merge_pos(row, 16 * j + 8 + gid);
+                *d0 = (k == 0 ? 0.f : *d0) + st.o[j][nt][c] * w;
+                *d1 = (k == 0 ? 0.f : *d1) + st.o[j][nt][c + 2] * w;
               } else {
-                d = 32 * gid + 2 * j;
-                v = make_float2(st.o[j][nt][c] * w, st.o[j][nt][c + 2] * w);
-              }
-              float2* dst = reinterpret_cast<float2*>(mbuf + merge_pos(row, d));
-              if (k == 0) {
-                *dst = v;
-              } else {
-                float2 acc = *dst;
-                acc.x += v.x;
-                acc.y += v.y;
-                *dst = acc;
+                int d;
+                float2 v;
+                if constexpr (KVDT != PNKV_KV_BF16) {
+                  const int mt = j & ~1;
+                  const int e = (j & 1) ? c + 2 : c;
+                  d = ((j & 1) ? 128 : 0) + 16 * gid + mt;
+                  v = make_float2(st.o[mt][nt][e] * w, st.o[mt + 1][nt][e] * w);
+                } else {
+                  d = 32 * gid + 2 * j;
+                  v = make_float2(st.o[j][nt][c] * w, st.o[j][nt][c + 2] * w);
+                }
+                float2* dst = reinterpret_cast<float2*>(mbuf + merge_pos(row, d));
+                if (k == 0) {
+                  *dst = v;
+                } else {
+                  float2 acc = *dst;
+                  acc.x += v.x;
+                  acc.y += v.y;
+                  *dst = acc;
+                }
               }
             }
           }

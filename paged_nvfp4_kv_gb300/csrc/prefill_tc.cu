@@ -393,7 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
     // ----------------------------------------------------------- dequant
     const int dt = threadIdx.x - kDequantWarp0 * 32;  // 0 .. 32 * kDequantWarps - 1
-    constexpr int kDT = 32 * kDequantWarps;
     int64_t gb = 0;
     bool ok = true;
     Tile t;

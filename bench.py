@@ -184,7 +184,7 @@ def tensor_peak():
 
 def workload(cfg):
     from paged_nvfp4_kv_gb300 import workloads as W
-    return W.CONFIGS[cfg]()
+    return W.WORKLOADS[cfg]()
 
 
 # ---------------------------------------------------------------------------
@@ -399,7 +399,7 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": algo_bytes}
     tile_path = int(w.qlen.max()) * (w.num_q_heads // w.num_kv_heads) > 64
     if tile_path:
-        # the tensor-core tile path: a dense contraction, judged against the
+        # the tensor-core tile path: a dense contraction, measured against the
         # tensor peak (QK^T and PV, 2 FLOP per multiply-add, causal-exact)
         flops = attention_flops(w)
         tflops = flops / (decode_ms * 1e-3) / 1e12

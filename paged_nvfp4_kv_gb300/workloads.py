@@ -234,6 +234,6 @@ def million_token_decode_int8(seed=1003):
     return build("million-token decode (1,048,576 INT8 group-64 keys)", seed, "int8", [1048575], [1])
 
 
-CONFIGS = {1: tiny_decode, 2: native_window_decode, 3: million_token_decode,
+WORKLOADS = {1: tiny_decode, 2: native_window_decode, 3: million_token_decode,
            4: multi_session_verify, 5: chunked_prefill, 6: chunked_prefill_reduced,
            7: million_token_decode_fp8, 8: million_token_decode_int8}

@@ -45,6 +45,8 @@ def parse():
                    help="workload number: 1..5 as in the workload table, 6 = reduced chunked prefill "
                         "(profiling), 7/8 = the million-token decode with an FP8/INT8 cache")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=1,
+                   help="also time a CUDA-graph replay of this many layers' steps (per-token latency)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     return p.parse_args()
 
@@ -424,6 +426,8 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "dev_err": err,
     }
+    if args.layers > 1:
+        line["layers_graph"] = layer_stack_ms(w, args.layers, K, W)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, dt = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_info(), "kind": "oracle",
@@ -434,6 +438,32 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def layer_stack_ms(w, layers, K, W):
+    """Per-token latency of ``layers`` attention layers (each its own pool,
+    append -> decode -> combine) replayed from one CUDA graph; CUDA events
+    around K replays after W warm-up replays."""
+    import torch
+    from paged_nvfp4_kv_gb300.engine import DecodeStack
+    st = DecodeStack(w, layers=layers)
+    st.fill()
+    st.capture()
+    for _ in range(W):
+        st.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        st.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    err = st.error_word()
+    del st
+    torch.cuda.empty_cache()
+    return {"layers": layers, "ms_per_token": ms, "ms_per_layer": ms / layers, "dev_err": err}
 
 
 def main():

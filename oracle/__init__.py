@@ -36,6 +36,8 @@ Modules:
   int8       INT8 group-64 quantise / dequantise (fp16 group scales).
   paged      page-pool byte layout, scatter and gather.
   attention  dense and paged attention, split-KV partials, LSE combine.
+  fp4_prefill  attention with NVFP4-quantised queries (the block-scaled
+             FP4 x FP4 QK^T reading of a prefill over the NVFP4 cache).
 
 Parity status: every function is pinned by a ``-m "not gpu"`` test against a
 closed form, an invariant, an exhaustive enumeration or brute force, except

@@ -253,7 +253,11 @@ int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads);
  * The pool must hold NVFP4, FP8, INT8 or bf16 pages with head_dim 256 and
  * 16-token pages; num_q_heads / num_kv_heads in 1..8 rows per query token.
  * More than 64 rows per KV head (a prefill chunk) run the tensor-core tile,
- * built for NVFP4 pools; other pools return PNKV_ERR_UNSUPPORTED there. */
+ * built for NVFP4 pools; other pools return PNKV_ERR_UNSUPPORTED there.
+ * The pool is read through a TMA map of 128-byte rows with 32-bit signed row
+ * coordinates: num_pages * num_kv_heads * rows per record (NVFP4 36, FP8 64,
+ * INT8 66, bf16 128) must stay below 2^31 (about 14.9M NVFP4 pages of 4 KV
+ * heads, 275 GB), else PNKV_ERR_INVALID_ARG. */
 int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q_roped,
                            const int32_t* qo_indptr, const int32_t* page_table,
                            int64_t pt_stride, const int32_t* seq_lens,

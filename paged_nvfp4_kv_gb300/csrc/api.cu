@@ -49,10 +49,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // The pool seen as a 2-D byte tensor [num_pages * hkv * box_rows][128].
 int make_pool_map(const pnkv_cache* c, int box_rows, void* map_out) {
   CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
-  if (!enc) return PNKV_ERR_CUDA;
   const cuuint64_t rows = static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * box_rows;
   if (rows >= (1ull << 31)) return PNKV_ERR_INVALID_ARG;  // TMA row coordinates are int32
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return PNKV_ERR_CUDA;
   const cuuint64_t dims[2] = {128, rows};
   const cuuint64_t strides[1] = {128};
   const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};

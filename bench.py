@@ -43,10 +43,17 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", type=int, default=3,
                    help="workload number: 1..5 as in the workload table, 6 = reduced chunked prefill "
-                        "(profiling), 7/8 = the million-token decode with an FP8/INT8 cache")
+                        "(profiling), 7/8 = the million-token decode with an FP8/INT8 cache, "
+                        "9 = reduced multi-session verify (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--layers", type=int, default=1,
-                   help="also time a CUDA-graph replay of this many layers' steps (per-token latency)")
+    p.add_argument("--layers", type=int, default=16,
+                   help="also time a CUDA-graph replay of this many layers' steps (per-token "
+                        "latency); 1 skips it")
+    p.add_argument("--fp4q", action="store_true",
+                   help="prefill workloads: NVFP4-encoded queries (block-scaled FP4 QK^T, "
+                        "paged_prefill_attention_fp4q) instead of bf16 queries")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads' records (the 'configs' object)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     return p.parse_args()
 
@@ -297,11 +304,131 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 
+def l2_flusher(torch, nbytes=512 << 20):
+    """A function that evicts L2 (129 MB on GB300) by writing a larger buffer."""
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    return lambda: buf.zero_()
+
+
+def measure_steps(s, K, W, stream, local, flush=None, q_scale=None):
+    """W warm-up steps, then K timed steps (append -> attention -> combine)
+    with CUDA events on the launching stream, and a second pass with events
+    between the three calls for per-kernel means.  With ``flush`` (inputs that
+    fit in L2) each step is timed on its own after an L2 flush outside its
+    events.  ``q_scale``: the FP4-query prefill instead of the bf16-query
+    attention."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            s.step(q_scale=q_scale)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    with clocks:
+        with torch.cuda.stream(stream):
+            if flush is None:
+                start = torch.cuda.Event(enable_timing=True)
+                stop = torch.cuda.Event(enable_timing=True)
+                start.record(stream)
+                for _ in range(K):
+                    s.step(q_scale=q_scale)
+                stop.record(stream)
+                stream.synchronize()
+                step_ms = start.elapsed_time(stop) / K
+            else:
+                evs = []
+                for _ in range(K):
+                    flush()
+                    e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    e[0].record(stream)
+                    s.step(q_scale=q_scale)
+                    e[1].record(stream)
+                    evs.append(e)
+                stream.synchronize()
+                step_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            if flush is not None:
+                flush()
+            ev[i][0].record(stream)
+            s.append()
+            ev[i][1].record(stream)
+            s.partials(q_scale)
+            ev[i][2].record(stream)
+            s.combine()
+            ev[i][3].record(stream)
+    stream.synchronize()
+    return {"step_ms": step_ms,
+            "append_ms": float(np.mean([e[0].elapsed_time(e[1]) for e in ev])),
+            "decode_ms": float(np.mean([e[1].elapsed_time(e[2]) for e in ev])),
+            "combine_ms": float(np.mean([e[2].elapsed_time(e[3]) for e in ev])),
+            "clocks": clocks.summary(), "dev_err": s.error_word()}
+
+
+def is_tile_path(w):
+    return int(w.qlen.max()) * (w.num_q_heads // w.num_kv_heads) > 64
+
+
+def roofline_of(w, decode_ms):
+    """Roofline of the step's dominant kernel: HBM bytes of KV + scales for
+    the split-KV decode, causal-exact QK^T + PV FLOPs for the tensor-core tile."""
+    keys = int(w.seq_lens.sum())
+    if is_tile_path(w):
+        flops = attention_flops(w)
+        tflops = flops / (decode_ms * 1e-3) / 1e12
+        tpeak, tkind = tensor_peak()
+        return {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": tflops / tpeak, "traffic": None, "peak_kind": tkind,
+                "kernel": "prefill_tile_kernel (tcgen05)", "algorithmic_flops_per_launch": flops}
+    peak, peak_kind = peaks()
+    algo_bytes = keys * ALGO_BYTES_PER_TOKEN[w.kv_dtype]
+    achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": profiled_traffic(w.kv_dtype) if keys == 1 << 20 else None,
+            "peak_kind": peak_kind, "kernel": "paged_decode_attention",
+            "algorithmic_bytes_per_launch": algo_bytes}
+
+
+def config_record(cfg, K, W, local, fp4q=False):
+    """One workload's step measured on its own (fill untimed): kernel times,
+    the dominant kernel's roofline, the clock record of its timed region.
+    ``fp4q``: the prefill chunk with NVFP4-encoded queries (block-scaled FP4
+    QK^T, paged_prefill_attention_fp4q) instead of bf16 queries."""
+    import torch
+    from paged_nvfp4_kv_gb300.engine import DecodeSession
+    w = workload(cfg)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        s = DecodeSession(w, device="cuda", stream=stream)
+        s.fill()
+    torch.cuda.synchronize()
+    pool_bytes = s.cache.pool.numel()
+    flush = l2_flusher(torch) if pool_bytes < (256 << 20) else None
+    m = measure_steps(s, K, W, stream, local, flush, q_scale=w.g_q if fp4q else None)
+    roof = roofline_of(w, m["decode_ms"])
+    keys = int(w.seq_lens.sum())
+    rec = {"workload": w.name + (", NVFP4 queries (block-scaled FP4 QK^T)" if fp4q else ""),
+           "kv_dtype": w.kv_dtype, "keys": keys,
+           "query_rows": int(w.total_q) * w.num_q_heads, "steps": K, "warmup": W,
+           "l2": "flushed before each step (pool fits in L2)" if flush else "pool larger than L2",
+           "step_ms": m["step_ms"],
+           "kernels_ms": {"kv_append_nvfp4": m["append_ms"], "paged_decode_attention": m["decode_ms"],
+                          "split_kv_combine": m["combine_ms"]},
+           "value": keys / (m["step_ms"] * 1e-3), "unit": UNIT,
+           "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_kind",
+                                             "kernel")},
+           "clocks": m["clocks"], "dev_err": m["dev_err"]}
+    del s
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     import torch
     import __graft_entry__
     __graft_entry__.build()
-    from paged_nvfp4_kv_gb300 import paged_decode_attention, split_kv_combine
     from paged_nvfp4_kv_gb300.engine import DecodeSession
 
     rank, world, local = dist_env()
@@ -317,51 +444,22 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K, W = args.steps, args.warmup
+    qs = w.g_q if (args.fp4q and is_tile_path(w)) else None
     with torch.cuda.stream(stream):
         for _ in range(W):
-            s.step()
+            s.step(q_scale=qs)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    # the headline: K whole steps back to back, events only around the loop
-    clocks = ClockSampler(local)
-    with clocks:
-        start = torch.cuda.Event(enable_timing=True)
-        stop = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(K):
-                s.step()
-            stop.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize()
-    # per-kernel times: a second pass with events between the three calls
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            ev[i][0].record(stream)
-            s.append()
-            ev[i][1].record(stream)
-            w_ = s.w
-            paged_decode_attention(s.cache, s.q_roped, s.qo_indptr, s.page_table, s.seq_lens,
-                                   w_.num_q_heads, s.max_qlen, s.sm_scale, w_.causal, s.o_part,
-                                   s.lse_part, s.work_meta, s.dev_err, stream)
-            ev[i][2].record(stream)
-            split_kv_combine(s.o_part, s.lse_part, s.work_meta, s.qo_indptr, s.total_q,
-                             w_.num_q_heads, w_.num_kv_heads, s.max_qlen, s.out, s.lse, stream)
-            ev[i][3].record(stream)
-    stream.synchronize()
+    # the headline: K whole steps back to back, events only around the loop,
+    # then the per-kernel pass (measure_steps; its warm-up is already done)
+    m = measure_steps(s, K, 0, stream, local, q_scale=qs)
     if world > 1:
         dist.barrier()
-    total_ms = replica_max(start.elapsed_time(stop), world, "cuda")
-    append_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
-    combine_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
-    ms_per_step = total_ms / K
+    ms_per_step = replica_max(m["step_ms"], world, "cuda")
     keys = int(w.seq_lens.sum())
     value = replica_rate(keys, ms_per_step, world)
-    err = s.error_word()
 
     # ---- end to end through the public API, host buffers
     qh = s.q.cpu().pin_memory()
@@ -375,7 +473,7 @@ def run_ours(args):
             s.q.copy_(qh, non_blocking=True)
             s.k.copy_(kh, non_blocking=True)
             s.v.copy_(vh, non_blocking=True)
-            s.step()
+            s.step(q_scale=qs)
             out_h.copy_(s.out, non_blocking=True)
         stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -385,49 +483,48 @@ def run_ours(args):
             s.q.copy_(qh, non_blocking=True)
             s.k.copy_(kh, non_blocking=True)
             s.v.copy_(vh, non_blocking=True)
-            s.step()
+            s.step(q_scale=qs)
             out_h.copy_(s.out, non_blocking=True)
         e1.record(stream)
         stream.synchronize()
     e2e_ms = replica_max(e0.elapsed_time(e1) / K, world, "cuda")
     e2e_value = replica_rate(keys, e2e_ms, world)
+    err = s.error_word()
 
-    peak, peak_kind = peaks()
-    algo_bytes = keys * ALGO_BYTES_PER_TOKEN[w.kv_dtype]
-    achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(w.kv_dtype),
-                "peak_kind": peak_kind, "kernel": "paged_decode_attention",
-                "algorithmic_bytes_per_launch": algo_bytes}
-    tile_path = int(w.qlen.max()) * (w.num_q_heads // w.num_kv_heads) > 64
-    if tile_path:
-        # the tensor-core tile path: a dense contraction, measured against the
-        # tensor peak (QK^T and PV, 2 FLOP per multiply-add, causal-exact)
-        flops = attention_flops(w)
-        tflops = flops / (decode_ms * 1e-3) / 1e12
-        tpeak, tkind = tensor_peak()
-        roofline = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": tflops / tpeak, "traffic": None, "peak_kind": tkind,
-                    "kernel": "prefill_tile_kernel (tcgen05)", "algorithmic_flops_per_launch": flops}
+    roofline = roofline_of(w, m["decode_ms"])
+    tile_path = is_tile_path(w)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16-mma/fp32-softmax over %s KV" % w.kv_dtype,
         "data": "synthetic",
-        "config": workload_config(w, world),
-        "kernels_ms": {"kv_append_nvfp4": append_ms, "paged_decode_attention": decode_ms,
-                       "split_kv_combine": combine_ms},
-        "hbm_gbs_decode": achieved,
+        "config": dict(workload_config(w, world), **({"queries": "NVFP4 (block-scaled FP4 QK^T)"} if qs else {})),
+        "kernels_ms": {"kv_append_nvfp4": m["append_ms"], "paged_decode_attention": m["decode_ms"],
+                       "split_kv_combine": m["combine_ms"]},
+        "hbm_gbs_decode": roofline["achieved"] if roofline["bound"] == "hbm" else None,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         # per step: append, decode (plus its metadata kernel on the tile path), combine
         "gpu_launches": (4 if tile_path else 3) * K,
-        "clocks": clocks.summary(),
+        "clocks": m["clocks"],
         "dev_err": err,
     }
+    del s
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     if args.layers > 1:
-        line["layers_graph"] = layer_stack_ms(w, args.layers, K, W)
+        line["layers_graph"] = layer_stack_ms(w, args.layers, max(K, 50), max(W, 3))
+    if not args.no_configs and world == 1:
+        # every other workload, measured on its own after the headline
+        recs = {}
+        for cfg in (1, 2, 4, 5, 7, 8):
+            if cfg == args.config:
+                continue
+            kc, wc = (3, 1) if cfg == 5 else (max(20, min(K, 200)), max(3, W))
+            recs[str(cfg)] = config_record(cfg, kc, wc, local)
+        recs["5-fp4q"] = config_record(5, 3, 1, local, fp4q=True)
+        line["configs"] = recs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, dt = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_info(), "kind": "oracle",
@@ -443,27 +540,32 @@ def run_ours(args):
 def layer_stack_ms(w, layers, K, W):
     """Per-token latency of ``layers`` attention layers (each its own pool,
     append -> decode -> combine) replayed from one CUDA graph; CUDA events
-    around K replays after W warm-up replays."""
+    around K replays after W warm-up replays.  The layers' pools start as
+    byte copies of one filled pool (the same work per layer; per-layer
+    contents are checked against the oracle by the graph tests)."""
     import torch
     from paged_nvfp4_kv_gb300.engine import DecodeStack
-    st = DecodeStack(w, layers=layers)
+    st = DecodeStack.replicated(w, layers)
     st.fill()
     st.capture()
     for _ in range(W):
         st.replay()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(K):
-        st.replay()
-    e1.record()
-    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    with clocks:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            st.replay()
+        e1.record()
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
     err = st.error_word()
     del st
     torch.cuda.empty_cache()
-    return {"layers": layers, "ms_per_token": ms, "ms_per_layer": ms / layers, "dev_err": err}
+    return {"layers": layers, "replays": K, "ms_per_token": ms, "ms_per_layer": ms / layers,
+            "launches_per_replay": 3 * layers, "clocks": clocks.summary(), "dev_err": err}
 
 
 def main():

@@ -15,10 +15,15 @@
  *   - Every pointer argument named as device memory must be device memory of
  *     the current CUDA device, allocated and owned by the caller; the library
  *     never allocates, frees or retains memory and keeps no state between
- *     calls (except a per-device cache of the device's SM count).
+ *     calls except a per-device cache of the device's SM count, the pipeline
+ *     wait bound (pnkv_set_wait_limit_ns) and the fixed scratch of
+ *     paged_decode_attention_noalloc.
  *   - Every call is asynchronous and stream-ordered on `stream` (a
  *     cudaStream_t; NULL is the legacy default stream).  A call returns once
  *     its kernels are enqueued.
+ *   - Kernel attributes (the shared-memory limit of the large kernels) are
+ *     set on the current device at its first call there, so one process may
+ *     drive several devices.
  *   - Return value: PNKV_OK, or a negative pnkv status.  Argument errors that
  *     the host can see return PNKV_ERR_INVALID_ARG before anything is
  *     launched; a failed launch returns PNKV_ERR_CUDA.
@@ -26,8 +31,12 @@
  *     past the page table or the rope table, a sequence longer than its page
  *     table row, an inconsistent qo_indptr, a pipeline wait that timed out)
  *     are OR-ed into the caller's device word `dev_err` (PNKV_DEV_ERR_* bits);
- *     the offending page or token is skipped and the kernel completes.  Read
- *     `dev_err` after synchronising the stream.
+ *     the offending page, token or sequence is skipped and the kernel
+ *     completes.  Read `dev_err` after synchronising the stream.  The outputs
+ *     of a flagged sequence are unspecified (a skipped sequence reads as no
+ *     visible key: zeros and LSE -inf); after a timeout all outputs of that
+ *     call are unspecified.  Other sequences' outputs are unaffected, and the
+ *     context stays usable.
  *   - bf16 tensors are passed as uint16_t bit patterns.
  *
  * Sources (pages on the method; the library restates them, it copies none):
@@ -65,7 +74,8 @@ enum {
   PNKV_DEV_ERR_PAGE_ID = 1,    /* page table entry outside [0, num_pages)    */
   PNKV_DEV_ERR_POSITION = 2,   /* token position >= rope table rows, or < 0  */
   PNKV_DEV_ERR_SEQ_LEN = 4,    /* position or seq_len beyond pt_stride * 16  */
-  PNKV_DEV_ERR_QO_INDPTR = 8,  /* qlen < 0, > max_qlen or > seq_len          */
+  PNKV_DEV_ERR_QO_INDPTR = 8,  /* qlen < 0, > max_qlen or > seq_len, or the
+                                  sequence's rows end past total_q          */
   PNKV_DEV_ERR_TIMEOUT = 16,   /* a bounded pipeline wait gave up            */
   PNKV_DEV_ERR_SEQ_INDEX = 32  /* tok_seq outside [0, batch)                 */
 };
@@ -236,9 +246,18 @@ int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads);
  * values (NVFP4, FP8, INT8: dequantised), softmax in fp32 with fp16 probabilities in
  * the P.V product.  Each split writes its normalised partial output and
  * natural-log LSE; empty splits write LSE = -inf.
+ * Query precision: on NVFP4, FP8 and INT8 pools the tensor-core products take
+ * the roped query in fp16 (the cache values are exact in fp16), so the
+ * query's bf16 elements must lie within the fp16 range (|q| <= 65,504); a
+ * larger element becomes infinite.  Elements below 2^-14 in magnitude keep
+ * fewer mantissa bits (fp16 subnormals; an error of at most 2^-25 per element),
+ * which the logit tolerance absorbs.  bf16 pools take the query unchanged.
  *
- *   q_roped     device bf16 [qo_indptr[batch], num_q_heads, 256]
- *   qo_indptr   device int32 [batch + 1], non-decreasing, qo_indptr[0] = 0
+ *   q_roped     device bf16 [total_q, num_q_heads, 256]
+ *   qo_indptr   device int32 [batch + 1], non-decreasing, qo_indptr[0] = 0,
+ *               qo_indptr[batch] <= total_q (a sequence whose rows end past
+ *               total_q is skipped and flagged PNKV_DEV_ERR_QO_INDPTR)
+ *   total_q     rows of q_roped (host copy of qo_indptr[batch])
  *   page_table  device int32 [batch, pt_stride]
  *   seq_lens    device int32 [batch]
  *   max_qlen    host bound on every qlen_b (1 .. 8192); num_q_heads /
@@ -261,10 +280,43 @@ int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads);
 int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q_roped,
                            const int32_t* qo_indptr, const int32_t* page_table,
                            int64_t pt_stride, const int32_t* seq_lens,
-                           int32_t batch, int32_t num_q_heads, int32_t max_qlen,
+                           int32_t batch, int64_t total_q, int32_t num_q_heads, int32_t max_qlen,
                            float sm_scale, int32_t causal, float* o_part,
                            float* lse_part, int64_t part_slots,
                            int32_t* work_meta, int32_t* dev_err, void* stream);
+
+/* Chunked prefill with NVFP4-encoded queries: the chunk's QK^T as a
+ * block-scaled FP4 x FP4 tensor-core product on the cache's own codes.
+ * ([NVFP4-page] "Why NVFP4 KV changes the math": K is E2M1 codes with an E4M3
+ * scale per 16 elements and an fp32 per-tensor scale -- the operand format of
+ * the block-scaled FP4 product; [YaRN-page] "Against vLLM: prefill loses,
+ * decode wins, and one surprise": the long-context engines prefill in
+ * chunks.  The pages print no such kernel; the query encoding below is this
+ * library's reading.)
+ *
+ * Same arguments, layouts and results as paged_decode_attention (partials,
+ * work_meta, dev_err, combine with split_kv_combine), except the logits:
+ * each roped bf16 query row is first encoded with the cache's NVFP4 encoder
+ * under the per-tensor decode scale q_scale (e = fp32(1 / (6 q_scale)); per
+ * 16-element block S = E4M3_rn_satfinite(fp32(amax * e)), zero block if
+ * E4M3(S) = 0, else codes E2M1_rn_satfinite(fp32(x * fp32(1 / fp32(E4M3(S) *
+ * q_scale))))), and z = (q_hat . k) * sm_scale with q_hat = E2M1(code) *
+ * E4M3(S) * q_scale, the query's round trip.  The block sums and their scaling
+ * are exact in binary32, so z equals the plain dot product of q_hat and the
+ * dequantised k up to the accumulation's rounding.  Softmax, P.V (fp16 P,
+ * dequantised V), LSE and the causal rule are paged_decode_attention's.
+ *   q_scale   per-tensor decode scale g_Q of the queries, in [2^-100, 2^100];
+ *             the caller calibrates it (e.g. amax(q) / (6 * 448))
+ * Only NVFP4 pools, and only requests with more than 64 query rows per KV
+ * head (num_q_heads / num_kv_heads * max_qlen > 64: a prefill chunk, the
+ * tensor-core tile path); anything else returns PNKV_ERR_UNSUPPORTED. */
+int paged_prefill_attention_fp4q(const pnkv_cache* cache, const uint16_t* q_roped,
+                                 const int32_t* qo_indptr, const int32_t* page_table,
+                                 int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                                 int64_t total_q, int32_t num_q_heads, int32_t max_qlen,
+                                 float sm_scale, int32_t causal, float q_scale, float* o_part,
+                                 float* lse_part, int64_t part_slots, int32_t* work_meta,
+                                 int32_t* dev_err, void* stream);
 
 /* Log-sum-exp merge of the split partials ([TP2-README] "Limitations",
  * split-KV decode; the merge is the standard one):
@@ -302,10 +354,13 @@ int split_kv_combine(const float* o_part, const float* lse_part,
  *   - Arguments and results are those of paged_decode_attention and
  *     split_kv_combine (total_q = qo_indptr[batch], host copy; out bf16, or
  *     fp32 when out_is_fp32; lse_out may be NULL).
- *   - Requests whose partials do not fit the scratch -- (batch * num_kv_heads
- *     + SM count) slots of num_q_heads / num_kv_heads * max_qlen rows of
- *     257 floats, plus the work metadata -- return PNKV_ERR_INVALID_ARG
- *     before anything is launched.
+ *   - Requests whose partials do not fit the scratch -- pnkv_decode_slots(...)
+ *     slots of num_q_heads / num_kv_heads * max_qlen rows of 257 floats, plus
+ *     the work metadata -- return PNKV_ERR_INVALID_ARG before anything is
+ *     launched.  On the split-KV path (at most 64 rows per KV head) the slot
+ *     count is batch * num_kv_heads + SM count; on the tensor-core tile path
+ *     (more rows) it is batch * num_kv_heads * key splits, which for a
+ *     prefill chunk of thousands of tokens normally exceeds the scratch.
  *   - The first call on a device looks up the scratch's device address with
  *     that device current; make that first call before any stream capture.
  *   - No scratch content needs to start at zero: each call writes every
@@ -321,6 +376,17 @@ int paged_decode_attention_noalloc(const pnkv_cache* cache, const uint16_t* q_ro
                                    int32_t causal, int64_t total_q, void* out,
                                    int32_t out_is_fp32, float* lse_out, int32_t* dev_err,
                                    void* stream);
+
+/* Bound, in nanoseconds, of every pipeline wait (an mbarrier wait between
+ * the roles of a CTA) in kernels launched after this call; returns the
+ * previous bound, or PNKV_ERR_INVALID_ARG for ns outside [1,000, 6e10].
+ * Default 2e9 (2 s): generous, because a shared GPU may be time-sliced.
+ * When a wait runs out the kernel sets PNKV_DEV_ERR_TIMEOUT in dev_err, its
+ * other warps stop at their next wait, and it returns; waits for bulk copies
+ * or MMAs already issued keep the 2 s bound, so no CTA exits with work in
+ * flight.  Process-wide, for every device; a diagnostic and test knob (a
+ * short bound makes ordinary waits run out). */
+int64_t pnkv_set_wait_limit_ns(int64_t ns);
 
 /* Static text for a status code. */
 const char* pnkv_status_string(int status);

@@ -13,8 +13,8 @@ from . import _lib
 from ._lib import PNKV_KV_BF16, PNKV_KV_FP8, PNKV_KV_INT8, PNKV_KV_NVFP4, CacheDesc, YarnParams
 
 __all__ = ["Cache", "YarnParams", "yarn_params", "yarn_rope_tables", "kv_append_nvfp4",
-           "paged_decode_attention", "split_kv_combine", "decode_slots", "work_meta_ints",
-           "page_bytes", "PNKV_KV_BF16", "PNKV_KV_NVFP4", "PNKV_KV_FP8", "PNKV_KV_INT8", "decode_dev_err"]
+           "paged_decode_attention", "paged_prefill_attention_fp4q", "split_kv_combine", "decode_slots", "work_meta_ints",
+           "page_bytes", "set_wait_limit_ns", "PNKV_KV_BF16", "PNKV_KV_NVFP4", "PNKV_KV_FP8", "PNKV_KV_INT8", "decode_dev_err"]
 
 _DTYPES = {"bf16": PNKV_KV_BF16, "nvfp4": PNKV_KV_NVFP4, "fp8": PNKV_KV_FP8, "int8": PNKV_KV_INT8}
 
@@ -114,10 +114,26 @@ def paged_decode_attention(cache, q_roped, qo_indptr, page_table, seq_lens, num_
     slots = lse_part.shape[0]
     st = _lib.load().paged_decode_attention(
         ctypes.byref(cache.desc), _ptr(q_roped), _ptr(qo_indptr), _ptr(page_table),
-        page_table.shape[1], _ptr(seq_lens), batch, int(num_q_heads), int(max_qlen),
+        page_table.shape[1], _ptr(seq_lens), batch, q_roped.shape[0], int(num_q_heads), int(max_qlen),
         float(sm_scale), 1 if causal else 0, _ptr(o_part), _ptr(lse_part), slots, _ptr(work_meta),
         _ptr(dev_err), _stream(stream))
     _lib.check(st, "paged_decode_attention")
+
+
+def paged_prefill_attention_fp4q(cache, q_roped, qo_indptr, page_table, seq_lens, num_q_heads,
+                                 max_qlen, sm_scale, causal, q_scale, o_part, lse_part, work_meta,
+                                 dev_err, stream=None):
+    """Prefill chunk with NVFP4-encoded queries (decode scale ``q_scale``):
+    block-scaled FP4 QK^T on the tensor cores; partials as for
+    paged_decode_attention."""
+    batch = seq_lens.numel()
+    slots = lse_part.shape[0]
+    st = _lib.load().paged_prefill_attention_fp4q(
+        ctypes.byref(cache.desc), _ptr(q_roped), _ptr(qo_indptr), _ptr(page_table),
+        page_table.shape[1], _ptr(seq_lens), batch, q_roped.shape[0], int(num_q_heads),
+        int(max_qlen), float(sm_scale), 1 if causal else 0, float(q_scale), _ptr(o_part),
+        _ptr(lse_part), slots, _ptr(work_meta), _ptr(dev_err), _stream(stream))
+    _lib.check(st, "paged_prefill_attention_fp4q")
 
 
 def split_kv_combine(o_part, lse_part, work_meta, qo_indptr, total_q, num_q_heads, num_kv_heads,
@@ -128,6 +144,15 @@ def split_kv_combine(o_part, lse_part, work_meta, qo_indptr, total_q, num_q_head
         int(num_q_heads), int(num_kv_heads), 256, int(max_qlen), _ptr(out),
         1 if out.dtype == torch.float32 else 0, _ptr(lse_out), _stream(stream))
     _lib.check(st, "split_kv_combine")
+
+
+def set_wait_limit_ns(ns):
+    """Bound of every pipeline wait in kernels launched from now on (a
+    diagnostic and test knob; default 2 s).  Returns the previous bound."""
+    v = _lib.load().pnkv_set_wait_limit_ns(int(ns))
+    if v < 0:
+        _lib.check(int(v), "pnkv_set_wait_limit_ns")
+    return int(v)
 
 
 def decode_dev_err(word):

@@ -51,13 +51,17 @@ SIGNATURES = [
     ("pnkv_decode_slots", _I64, [ctypes.POINTER(CacheDesc), _I32, _I32, _I32]),
     ("pnkv_work_meta_ints", _I64, [_I32, _I32]),
     ("paged_decode_attention", ctypes.c_int,
-     [ctypes.POINTER(CacheDesc), _P, _P, _P, _I64, _P, _I32, _I32, _I32, _F, _I32, _P, _P, _I64,
-      _P, _P, _P]),
+     [ctypes.POINTER(CacheDesc), _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _F, _I32, _P, _P,
+      _I64, _P, _P, _P]),
+    ("paged_prefill_attention_fp4q", ctypes.c_int,
+     [ctypes.POINTER(CacheDesc), _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _F, _I32, _F, _P,
+      _P, _I64, _P, _P, _P]),
     ("split_kv_combine", ctypes.c_int,
      [_P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _I32, _P, _P]),
     ("paged_decode_attention_noalloc", ctypes.c_int,
      [ctypes.POINTER(CacheDesc), _P, _P, _P, _I64, _P, _I32, _I32, _I32, _F, _I32, _I64, _P, _I32,
       _P, _P, _P]),
+    ("pnkv_set_wait_limit_ns", _I64, [_I64]),
     ("pnkv_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("pnkv_version", ctypes.c_int, []),
 ]

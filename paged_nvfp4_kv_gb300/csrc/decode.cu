@@ -42,9 +42,9 @@ namespace pnkv {
 
 int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32_t* qo_indptr,
                    const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
-                   int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal, float* o_part,
-                   float* lse_part, int64_t part_slots, int32_t* work_meta, int32_t* dev_err,
-                   cudaStream_t stream);
+                   int64_t total_q, int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal,
+                   float q_scale, float* o_part, float* lse_part, int64_t part_slots, int32_t* work_meta,
+                   int32_t* dev_err, cudaStream_t stream);
 int prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t max_qlen, int sms);
 
 namespace {
@@ -78,10 +78,12 @@ struct DecodeArgs {
   int64_t pt_stride;
   const int32_t* seq_lens;
   int32_t batch;
+  int64_t total_q;        // rows of q (qo_indptr[batch] must not exceed it)
   int32_t hq;
   int32_t max_qlen;
   int32_t rows_per_slot;  // group * max_qlen
   int32_t causal;
+  uint64_t wait_ns;       // bound of a pipeline wait
   float* o_part;
   float* lse_part;
   int64_t part_slots;
@@ -134,7 +136,8 @@ __device__ __forceinline__ SeqInfo load_seq(const DecodeArgs& a, int b, bool fla
   s.qlen = __ldg(a.qo_indptr + b + 1) - s.q0;
   s.pages = (s.len + 15) >> 4;
   bool ok = true;
-  if (s.qlen < 0 || s.qlen > a.max_qlen || s.qlen > s.len || s.q0 < 0) {
+  if (s.qlen < 0 || s.qlen > a.max_qlen || s.qlen > s.len || s.q0 < 0 ||
+      static_cast<int64_t>(s.q0) + s.qlen > a.total_q) {
     if (flag) flag_error(a.dev_err, PNKV_DEV_ERR_QO_INDPTR);
     ok = false;
   }
@@ -258,9 +261,10 @@ struct Plan {
   static constexpr int kMergeBytes = kRows * 256 * 4;
   static constexpr int kMlBytes = kStreams * kRows * 2 * 4;
   static constexpr int kQBytes = QS ? NTW * RG * 16 * 32 * 8 : 0;  // Q fragments in shared memory
-  static constexpr int kFixed = kMergeBytes + kMlBytes + kQBytes + 1024 /*align*/ + 1024 /*bars, flags*/;
+  // per stage: its bytes plus two mbarriers and two int32 (valid, armed)
+  static constexpr int kFixed = kMergeBytes + kMlBytes + kQBytes + 1024 /*align*/ + 64 /*flags, padding*/;
   static constexpr int kMaxSmem = 232448;
-  static constexpr int kStagesFit = (kMaxSmem - kFixed) / Geometry<KVDT>::kStageBytes;
+  static constexpr int kStagesFit = (kMaxSmem - kFixed) / (Geometry<KVDT>::kStageBytes + 24);
 #ifndef PNKV_MAX_STAGES
 #define PNKV_MAX_STAGES 48
 #endif
@@ -269,8 +273,10 @@ struct Plan {
   static constexpr int kStageRegion = kStages * Geometry<KVDT>::kStageBytes;
   static constexpr int kBarOff = kStageRegion;                 // full[S], empty[S]
   static constexpr int kMetaOff = kBarOff + 2 * 8 * kStages;   // int32 valid[S]
-  static constexpr int kAbortOff = kMetaOff + 4 * kStages;     // int32 abort flag
-  static constexpr int kMlOff = (kAbortOff + 4 + 15) & ~15;
+  static constexpr int kArmOff = kMetaOff + 4 * kStages;       // int32 armed[S]: unit that armed the stage
+  static constexpr int kAbortOff = kArmOff + 4 * kStages;      // int32 abort flag
+  static constexpr int kPieceAbortOff = kAbortOff + 4;         // the flag as seen at a piece's end
+  static constexpr int kMlOff = (kPieceAbortOff + 4 + 15) & ~15;
   static constexpr int kMergeOff = (kMlOff + kMlBytes + 15) & ~15;
   static constexpr int kQOff = kMergeOff + kMergeBytes;
   static constexpr int kTotal = kQOff + kQBytes;
@@ -855,7 +861,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kBarOff);
   uint64_t* empty = full + P::kStages;
   int32_t* stage_valid = reinterpret_cast<int32_t*>(smem + P::kMetaOff);
+  int32_t* stage_armed = reinterpret_cast<int32_t*>(smem + P::kArmOff);
   volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + P::kAbortOff);
+  volatile int32_t* piece_abort = reinterpret_cast<int32_t*>(smem + P::kPieceAbortOff);
   float* ml = reinterpret_cast<float*>(smem + P::kMlOff);
   float* mbuf = reinterpret_cast<float*>(smem + P::kMergeOff);
 
@@ -866,6 +874,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int s = 0; s < P::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], RG);
+      stage_armed[s] = -1;
     }
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -902,6 +911,21 @@ __global__ void __launch_bounds__(NW * 32, 1)
   walk.init(a, u_begin, u_end, lane);
   Piece pc;
 
+  // the CTA holding a segment's first unit records where the segment's slots
+  // are, before any work (so the record exists even if the call winds down
+  // after a timeout)
+  if (threadIdx.x == 0) {
+    Walker w0 = walk;
+    while (w0.next(a, &pc)) {
+      if (pc.p0 != 0) continue;
+      const int64_t seg = pc.b * static_cast<int64_t>(a.hkv) + pc.h;
+      const int64_t first_cta = pc.seg_start / chunk;
+      const int64_t last_cta = (pc.seg_start + pc.s.pages - 1) / chunk;
+      a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg + first_cta);
+      a.work_meta[4 + 2 * seg + 1] = static_cast<int32_t>(last_cta - first_cta + 1);
+    }
+  }
+
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
@@ -921,14 +945,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
             const int64_t i = issued + lane;
             const int s = static_cast<int>(i % P::kStages);
             const uint32_t par = static_cast<uint32_t>((i / P::kStages) & 1) ^ 1u;
-            if (*abort_flag || !mbar_wait(&empty[s], par)) {
-              lane_ok = false;
+            if (*abort_flag || !mbar_wait(&empty[s], par, a.wait_ns)) {
+              lane_ok = false;  // nothing armed: the drain skips this unit
             } else if (page < 0 || page >= a.num_pages) {
               flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
               stage_valid[s] = 0;
+              stage_armed[s] = static_cast<int32_t>(i);
               mbar_arrive(&full[s]);
             } else {
               stage_valid[s] = 1;
+              stage_armed[s] = static_cast<int32_t>(i);
               mbar_arrive_expect_tx(&full[s], Geo::kTxBytes);
               const int32_t y = (page * a.hkv + pc.h) * Geo::kBoxRows;
               tma_load_2d(smem + s * Geo::kStageBytes, &tmap, 0, y, &full[s], policy);
@@ -947,10 +973,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     }
     if (!ok && lane == 0) {
-      // drain: wait (bounded) for the loads that may still be in flight
+      // drain: wait (with the fixed bound) for the loads that may still be in
+      // flight, so the CTA never exits with a bulk copy landing; a unit whose
+      // stage was never armed (its lane gave up first) has nothing to wait for
       const int64_t first = issued > P::kStages ? issued - P::kStages : 0;
       for (int64_t i = first; i < issued; ++i)
-        mbar_wait(&full[i % P::kStages], static_cast<uint32_t>((i / P::kStages) & 1));
+        if (stage_armed[i % P::kStages] == static_cast<int32_t>(i))
+          mbar_wait(&full[i % P::kStages], static_cast<uint32_t>((i / P::kStages) & 1));
     }
     return;
   }
@@ -1018,8 +1047,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
           par ^= 1u;
         }
         st_idx[pg] = idx;
-        if (okw && here[pg]) okw = mbar_wait(&full[idx], par);
+        if (okw && here[pg]) okw = mbar_wait(&full[idx], par, a.wait_ns);
       }
+      // one outcome per warp: the MMAs below need every lane
+      okw = __all_sync(0xffffffffu, okw);
       i_stage += NP * static_cast<int>(S);
       if (i_stage >= P::kStages) {
         i_stage -= P::kStages;
@@ -1165,16 +1196,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
         if (d4 == 0) a.lse_part[slot * a.rows_per_slot + row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
       }
     }
-    // 5. the CTA holding the segment's first unit records where its slots are
-    if (threadIdx.x == 0 && pc.p0 == 0) {
-      const int64_t seg = pc.b * static_cast<int64_t>(a.hkv) + pc.h;
-      const int64_t first_cta = pc.seg_start / chunk;
-      const int64_t last_cta = (pc.seg_start + pc.s.pages - 1) / chunk;
-      a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg + first_cta);
-      a.work_meta[4 + 2 * seg + 1] = static_cast<int32_t>(last_cta - first_cta + 1);
-    }
+    // every consumer warp takes the same decision: the flag (which the
+    // producer may set at any time) is sampled once, before the barrier, and
+    // read after it (the next sample comes after further barriers)
+    if (threadIdx.x == 0) *piece_abort = *abort_flag;
     named_bar_sync(1, C::kThreads);
-    if (*abort_flag) break;
+    if (*piece_abort) break;
   }
 }
 
@@ -1188,13 +1215,9 @@ template <int KVDT, int NTW, int RG, int NW, int QS = 0, int NP = (NTW > 1 ? 2 :
 int launch_decode(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
   using P = Plan<KVDT, NTW, RG, NW, QS>;
   auto kern = paged_decode_kernel<KVDT, NTW, RG, NW, QS, NP>;
-  static bool configured = false;  // attribute set once per process (idempotent)
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kDynamicBytes) !=
-        cudaSuccess)
-      return PNKV_ERR_CUDA;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // devices whose attribute is set
+  const int st = set_smem_limit_once(configured, reinterpret_cast<const void*>(kern), P::kDynamicBytes);
+  if (st != PNKV_OK) return st;
   return launch_pdl(kern, dim3(grid), dim3(NW * 32), P::kDynamicBytes, stream, map, a);
 }
 
@@ -1260,7 +1283,7 @@ extern "C" int64_t pnkv_work_meta_ints(int32_t batch, int32_t num_kv_heads) {
 extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q_roped,
                                       const int32_t* qo_indptr, const int32_t* page_table,
                                       int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
-                                      int32_t num_q_heads, int32_t max_qlen, float sm_scale,
+                                      int64_t total_q, int32_t num_q_heads, int32_t max_qlen, float sm_scale,
                                       int32_t causal, float* o_part, float* lse_part, int64_t part_slots,
                                       int32_t* work_meta, int32_t* dev_err, void* stream) {
   using namespace pnkv;
@@ -1269,7 +1292,7 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   if (!q_roped || !qo_indptr || !page_table || !seq_lens || !o_part || !lse_part || !work_meta || !dev_err)
     return PNKV_ERR_INVALID_ARG;
   if (batch < 1 || pt_stride < 1 || max_qlen < 1 || max_qlen > 8192 || num_q_heads < 1 ||
-      num_q_heads % cache->num_kv_heads != 0)
+      num_q_heads % cache->num_kv_heads != 0 || total_q < 0)
     return PNKV_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return PNKV_ERR_INVALID_ARG;
   if (!aligned(q_roped, 16) || !aligned(o_part, 16) || !aligned(lse_part, 4)) return PNKV_ERR_INVALID_ARG;
@@ -1277,9 +1300,9 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   if (group > 8) return PNKV_ERR_UNSUPPORTED;
   const int64_t rows_per_slot = static_cast<int64_t>(group) * max_qlen;
   if (rows_per_slot > 64)  // many query rows per KV head: the tensor-core tile path
-    return launch_prefill(cache, q_roped, qo_indptr, page_table, pt_stride, seq_lens, batch, num_q_heads,
-                          max_qlen, sm_scale, causal, o_part, lse_part, part_slots, work_meta, dev_err,
-                          as_stream(stream));
+    return launch_prefill(cache, q_roped, qo_indptr, page_table, pt_stride, seq_lens, batch, total_q,
+                          num_q_heads, max_qlen, sm_scale, causal, 0.f, o_part, lse_part, part_slots,
+                          work_meta, dev_err, as_stream(stream));
   int grid = 0;
   if ((st = decode_grid(&grid)) != PNKV_OK) return st;
   if (part_slots < static_cast<int64_t>(batch) * cache->num_kv_heads + grid) return PNKV_ERR_INVALID_ARG;
@@ -1298,10 +1321,12 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   a.pt_stride = pt_stride;
   a.seq_lens = seq_lens;
   a.batch = batch;
+  a.total_q = total_q;
   a.hq = num_q_heads;
   a.max_qlen = max_qlen;
   a.rows_per_slot = static_cast<int32_t>(rows_per_slot);
   a.causal = causal ? 1 : 0;
+  a.wait_ns = pipeline_wait_ns();
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.part_slots = part_slots;
@@ -1319,4 +1344,33 @@ extern "C" int paged_decode_attention(const pnkv_cache* cache, const uint16_t* q
   if (cache->dtype == PNKV_KV_FP8) return dispatch_rows<PNKV_KV_FP8>(map, a, grid, s);
   if (cache->dtype == PNKV_KV_INT8) return dispatch_rows<PNKV_KV_INT8>(map, a, grid, s);
   return dispatch_rows<PNKV_KV_BF16>(map, a, grid, s);
+}
+
+extern "C" int paged_prefill_attention_fp4q(const pnkv_cache* cache, const uint16_t* q_roped,
+                                           const int32_t* qo_indptr, const int32_t* page_table,
+                                           int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                                           int64_t total_q, int32_t num_q_heads, int32_t max_qlen,
+                                           float sm_scale, int32_t causal, float q_scale, float* o_part,
+                                           float* lse_part, int64_t part_slots, int32_t* work_meta,
+                                           int32_t* dev_err, void* stream) {
+  using namespace pnkv;
+  int st = check_cache(cache);
+  if (st != PNKV_OK) return st;
+  if (!q_roped || !qo_indptr || !page_table || !seq_lens || !o_part || !lse_part || !work_meta || !dev_err)
+    return PNKV_ERR_INVALID_ARG;
+  if (batch < 1 || pt_stride < 1 || max_qlen < 1 || max_qlen > 8192 || num_q_heads < 1 ||
+      num_q_heads % cache->num_kv_heads != 0 || total_q < 0)
+    return PNKV_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return PNKV_ERR_INVALID_ARG;
+  // the query encoder's scales must stay normal in binary32, as the cache's do
+  if (!std::isfinite(q_scale) || !(q_scale >= 0x1p-100f) || !(q_scale <= 0x1p100f)) return PNKV_ERR_INVALID_ARG;
+  if (!aligned(q_roped, 16) || !aligned(o_part, 16) || !aligned(lse_part, 4)) return PNKV_ERR_INVALID_ARG;
+  const int group = num_q_heads / cache->num_kv_heads;
+  if (group > 8) return PNKV_ERR_UNSUPPORTED;
+  // the block-scaled product is the tile path's: at most 64 rows per KV head
+  // (a decode step) stay with paged_decode_attention
+  if (static_cast<int64_t>(group) * max_qlen <= 64) return PNKV_ERR_UNSUPPORTED;
+  return launch_prefill(cache, q_roped, qo_indptr, page_table, pt_stride, seq_lens, batch, total_q, num_q_heads,
+                        max_qlen, sm_scale, causal, q_scale, o_part, lse_part, part_slots, work_meta, dev_err,
+                        as_stream(stream));
 }

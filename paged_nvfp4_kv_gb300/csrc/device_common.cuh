@@ -23,9 +23,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// A pipeline wait gives up after this long (the GPU is shared and may be
-// time-sliced, so the bound is generous); the kernel then flags
-// PNKV_DEV_ERR_TIMEOUT and winds down instead of hanging.
+// Default bound of a pipeline wait (the GPU is shared and may be
+// time-sliced, so the bound is generous); on expiry the kernel flags
+// PNKV_DEV_ERR_TIMEOUT and winds down instead of hanging.  Pipeline waits
+// take their bound from the launch arguments (pnkv_set_wait_limit_ns); the
+// waits of a wind-down -- for bulk copies or MMAs already issued, which always
+// complete -- keep this bound, so that no CTA exits with work in flight.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // -------------------------------------------------------------- mbarrier --
@@ -66,13 +69,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and the caller flags a timeout) if that takes longer than kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// (and the caller flags a timeout) if that takes longer than limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -246,6 +249,39 @@ __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
+}
+
+// ------------------------------------------------------- NVFP4 encoding --
+// The two-level NVFP4 encoder of the cache ("262,144 Tokens on One RTX 5090",
+// section "Why NVFP4 KV changes the math": E2M1 codes with an E4M3 scale per
+// 16 elements and one fp32 decode scale g per tensor), shared by the cache
+// writer and the FP4-query prefill tile so that both round identically.
+
+// E2M1 code of a binary32 value: round to nearest, ties to the even code,
+// saturate at 6; the sign bit is the value's (so -0 and tiny negatives give
+// code 8).  Thresholds are the midpoints of {0, .5, 1, 1.5, 2, 3, 4, 6}; at a
+// midpoint the even code wins (codes 0, 2, 4, 6 hold 0, 1, 2, 4).
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float m = fabsf(y);
+  uint32_t c = (m > 0.25f) + (m >= 0.75f) + (m > 1.25f) + (m >= 1.75f) + (m > 2.5f) + (m >= 3.5f) +
+               (m > 5.0f);
+  return c | ((__float_as_uint(y) >> 31) << 3);
+}
+
+// Scale byte of a 16-element block whose largest magnitude is amax, for the
+// decode scale g and enc = fp32(1 / (6 g)): S = E4M3_rn_satfinite(fp32(amax *
+// enc)); 0 when E4M3(S) is zero (the block's codes are then all zero).
+// Otherwise *r = fp32(1 / fp32(E4M3(S) * g)), the factor the codes are
+// rounded from: code_i = E2M1(fp32(x_i * r)).
+__device__ __forceinline__ uint32_t nvfp4_block_scale(float amax, float g, float enc, float* r) {
+  const uint32_t s = f32_to_e4m3_satfinite(__fmul_rn(amax, enc));
+  const float sdec = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_to_f16x2(s) & 0xFFFFu)));
+  if (sdec == 0.f) {
+    *r = 0.f;
+    return 0u;
+  }
+  *r = __frcp_rn(__fmul_rn(sdec, g));
+  return s;
 }
 
 // Byte offset of (row, byte) inside a tile written by a 2-D TMA load with

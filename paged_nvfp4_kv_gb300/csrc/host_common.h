@@ -2,6 +2,7 @@
 // launch-error mapping and the per-device SM count.
 #pragma once
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <utility>
@@ -45,10 +46,33 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 // SM count of the current device (cached per device id).
 int device_sm_count(int* out_sms);
 
+// Bound, in nanoseconds, that kernels launched from now on give their
+// pipeline waits (pnkv_set_wait_limit_ns).
+uint64_t pipeline_wait_ns();
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device that is current when it is
+// set, so it is set once per device; `done` (one static per kernel) records
+// the devices (ids below 64; higher ids set it on every call).  Two threads
+// racing on a device's first call both set it, which is harmless.
+inline int set_smem_limit_once(std::atomic<uint64_t>& done, const void* kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PNKV_ERR_CUDA;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return PNKV_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return PNKV_ERR_CUDA;
+  if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return PNKV_OK;
+}
+
 // The pool as a 2-D byte tensor [num_pages * num_kv_heads * box_rows][128]
 // with a box of box_rows x 128 bytes and 128-byte swizzling (one head record
 // of a page per box); written to *map (a CUtensorMap).
 int make_pool_map(const pnkv_cache* c, int box_rows, void* map);
+
+// Same with records of record_rows rows read in boxes of box_rows rows.
+int make_pool_map_box(const pnkv_cache* c, int record_rows, int box_rows, void* map);
 
 // Pool geometry checks shared by every call that touches the pool.
 inline int check_cache(const pnkv_cache* c) {

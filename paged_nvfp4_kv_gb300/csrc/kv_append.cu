@@ -55,17 +55,6 @@ struct AppendArgs {
   int32_t* dev_err;
 };
 
-// E2M1 code of a binary32 value: round to nearest, ties to the even code,
-// saturate at 6; the sign bit is the value's (so -0 and tiny negatives give
-// code 8).  Thresholds are the midpoints of {0, .5, 1, 1.5, 2, 3, 4, 6}; at a
-// midpoint the even code wins (codes 0, 2, 4, 6 hold 0, 1, 2, 4).
-__device__ __forceinline__ uint32_t e2m1_code(float y) {
-  const float m = fabsf(y);
-  uint32_t c = (m > 0.25f) + (m >= 0.75f) + (m > 1.25f) + (m >= 1.75f) + (m > 2.5f) + (m >= 3.5f) +
-               (m > 5.0f);
-  return c | ((__float_as_uint(y) >> 31) << 3);
-}
-
 // E4M3 code of a binary32 value: round to nearest even, saturate at 448; the
 // sign bit is the value's (tiny negatives give code 0x80 whatever the
 // conversion does with the sign of a zero result).
@@ -112,18 +101,13 @@ __device__ __forceinline__ uint32_t quantize8(const float (&x)[8], float g, uint
   for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
   const float enc = __double2float_rn(1.0 / (6.0 * static_cast<double>(g)));
-  uint32_t s = f32_to_e4m3_satfinite(__fmul_rn(a, enc));
-  const float sdec = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_to_f16x2(s) & 0xFFFFu)));
+  float r;
+  *scale_byte = nvfp4_block_scale(a, g, enc, &r);
   uint32_t codes = 0;
-  if (sdec != 0.f) {
-    const float d = __fmul_rn(sdec, g);
-    const float r = __frcp_rn(d);
+  if (*scale_byte != 0) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) codes |= e2m1_code(__fmul_rn(x[e], r)) << (4 * e);
-  } else {
-    s = 0;
   }
-  *scale_byte = s;
   return codes;
 }
 

@@ -10,6 +10,8 @@
 // that lives in the library's own device memory (every GPU that loads the
 // library holds it until the process exits) and otherwise runs exactly the
 // regular decode and combine kernels.
+#include <mutex>
+
 #include "host_common.h"
 
 namespace pnkv {
@@ -19,14 +21,17 @@ namespace {
 static __device__ __align__(256) unsigned char g_scratch[PNKV_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and then reused.
+// per device (with that device current) and then reused; the lock makes the
+// first calls of several host threads safe.
 int scratch_for_current_device(unsigned char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PNKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return PNKV_ERR_CUDA;
@@ -70,7 +75,7 @@ extern "C" int paged_decode_attention_noalloc(const pnkv_cache* cache, const uin
   float* lse_part = reinterpret_cast<float*>(base + meta_bytes);
   float* o_part = reinterpret_cast<float*>(base + meta_bytes + lse_bytes);
   st = paged_decode_attention(cache, q_roped, qo_indptr, page_table, pt_stride, seq_lens, batch,
-                              num_q_heads, max_qlen, sm_scale, causal, o_part, lse_part, slots,
+                              total_q, num_q_heads, max_qlen, sm_scale, causal, o_part, lse_part, slots,
                               meta, dev_err, stream);
   if (st != PNKV_OK) return st;
   return split_kv_combine(o_part, lse_part, meta, qo_indptr, batch, total_q, num_q_heads,

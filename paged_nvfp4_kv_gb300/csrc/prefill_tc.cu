@@ -33,7 +33,20 @@
 // decode path.  The CTA writes one normalised partial (with its natural-log
 // LSE) per row into the (sequence, KV head) slot, which split_kv_combine
 // passes through.
+//
+// FP4-query variant (paged_prefill_attention_fp4q).  The cache's K codes are
+// E2M1 with an E4M3 scale per 16 elements ("262,144 Tokens on One RTX 5090",
+// section "Why NVFP4 KV changes the math"), which is the operand format of
+// the block-scaled FP4 tensor-core product.  With the queries encoded the
+// same way (the cache's own encoder, a caller-given per-tensor decode scale
+// g_Q), S = Q K^T runs as tcgen05.mma kind::mxf4nvf4 (K 64 per instruction,
+// E4M3 scales per 16 elements applied inside the product) straight on the
+// codes: each page's 16 rows of K codes are TMA-loaded into a contiguous
+// 128-byte-swizzled B tile, the K scales go to TMEM, and nothing of K is
+// widened.  The logits are then (q_hat . k_hat) * sm_scale with q_hat the
+// queries' NVFP4 round trip; P V is unchanged.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -53,72 +66,113 @@ constexpr int kMmaWarp = 13;          // issues P V; allocates TMEM
 constexpr int kQkWarp = 14;           // issues QK
 constexpr int kBlockKeys = 64;        // keys per KV block (four pages)
 constexpr int kBlockPages = kBlockKeys / 16;
-// ring depths.  The QK of block g waits for the softmax of block g - kSStages
-// to have loaded its S slot, so QK runs up to kSStages blocks ahead of the
-// softmax, and the softmax of a block overlaps the P V of the one before.
-constexpr int kRawStages = 3;
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
-constexpr int kSStages = 2;
-constexpr int kPStages = 2;
-constexpr int kRawPageBytes = 5120;   // 4,608-byte record, 1,024-aligned slot
-constexpr int kRawStageBytes = kBlockPages * kRawPageBytes;
-constexpr uint32_t kRecBytes = 4608;
+constexpr uint32_t kRecBytes = 4608;  // one NVFP4 head record (36 rows of 128 B)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
-// Shared memory plan (offsets from a 1,024-byte aligned base).  Q lives in
-// TMEM (the A operand of S = Q K^T), so shared memory holds only the streamed
-// operands.
-constexpr int kKOff = 0;                                  // ring of [64 x 256] fp16
-constexpr int kKBytes = kBlockKeys * 256 * 2;
-constexpr int kVOff = kKOff + kKStages * kKBytes;         // ring of [256 x 64] fp16
-constexpr int kVBytes = 256 * kBlockKeys * 2;
-constexpr int kPOff = kVOff + kVStages * kVBytes;         // ring of [128 x 64] fp16
-constexpr int kPBytes = 128 * kBlockKeys * 2;
-constexpr int kRawOff = kPOff + kPStages * kPBytes;       // raw NVFP4 records
-constexpr int kScrOff = kRawOff + kRawStages * kRawStageBytes;  // per dequant warp: V scales
-constexpr int kScrWarpBytes = kBlockPages * 32;                 // [page][2 blocks][16 slots]
-constexpr int kBarOff = kScrOff + kDequantWarps * kScrWarpBytes;
-enum {
-  B_RAW_FULL = 0,
-  B_RAW_EMPTY = B_RAW_FULL + kRawStages,
-  B_K_FULL = B_RAW_EMPTY + kRawStages,
-  B_K_FREE = B_K_FULL + kKStages,
-  B_V_FULL = B_K_FREE + kKStages,
-  B_V_FREE = B_V_FULL + kVStages,
-  B_S_FULL = B_V_FREE + kVStages,
-  B_S_FREE = B_S_FULL + kSStages,
-  B_P_FULL = B_S_FREE + kSStages,
-  B_PV_DONE = B_P_FULL + kPStages,
-  B_Q_FULL = B_PV_DONE + kPStages,
-  B_FINAL = B_Q_FULL + 1,
-  kNumBars = B_FINAL + 1
-};
-constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort, raw valid[]
-constexpr int kSmemBytes = kMiscOff + 64 + 1024;
-static_assert(kSmemBytes <= 232448, "prefill shared memory plan too large");
+// Shared-memory and TMEM plan of each variant (offsets from a 1,024-byte
+// aligned base).  Ring depths: the QK of block g waits for the softmax of
+// block g - kSStages to have loaded its S slot, so QK runs up to kSStages
+// blocks ahead of the softmax, and the softmax of a block overlaps the P V of
+// the one before.
+template <bool FP4Q>
+struct Plan;
 
-// TMEM columns: the S ring at 0 and 64; O at 128 .. 383; Q (fp16, two per
-// 32-bit column) at 384 .. 511.
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = kSStages * kBlockKeys;
-constexpr uint32_t kTmemQ = kTmemO + 256;
-static_assert(kTmemQ + 128 <= kTmemCols, "TMEM plan too large");
+// fp16 QK: the raw ring holds whole head records (one 36-row TMA box per
+// page); K is widened into an fp16 ring; Q (fp16) lives in TMEM.
+template <>
+struct Plan<false> {
+  static constexpr int kRawStages = 3, kKStages = 2, kVStages = 2, kSStages = 2, kPStages = 2;
+  static constexpr int kRawRows = 36;                    // record rows in a raw page slot
+  static constexpr int kRawRow0 = 0;                     // record row of raw row 0
+  static constexpr int kRawPageBytes = 5120;             // 4,608-byte record, 1,024-aligned slot
+  static constexpr uint32_t kRawTx = kRecBytes;
+  static constexpr int kKBytes = kBlockKeys * 256 * 2;   // fp16 [64 keys][256 dims]
+  static constexpr int kQBytes = 0, kSfaXBytes = 0;
+  static constexpr uint32_t kTmemQ = 384;                // fp16 Q, two per column: 384 .. 511
+  static constexpr uint32_t kTmemSfb = 0;
+};
+
+// FP4 QK: K codes go straight from the pool into an FP4 ring (one 16-row TMA
+// box per page); the raw ring holds the records' other 20 rows (K scales, V
+// codes, V scales); Q codes live in shared memory, the scale factors in TMEM.
+template <>
+struct Plan<true> {
+  static constexpr int kRawStages = 4, kKStages = 3, kVStages = 2, kSStages = 2, kPStages = 2;
+  static constexpr int kRawRows = 20;
+  static constexpr int kRawRow0 = 16;
+  static constexpr int kRawPageBytes = 3072;             // 2,560 bytes, 1,024-aligned slot
+  static constexpr uint32_t kRawTx = 20 * 128;
+  static constexpr int kKBytes = kBlockKeys * 128;       // E2M1 codes [64 keys][128 B], SW128
+  static constexpr int kQBytes = 128 * 128;              // E2M1 codes [128 rows][128 B], SW128
+  static constexpr int kSfaXBytes = 128 * 16;            // Q scale bytes [128 rows][16]
+  static constexpr uint32_t kTmemQ = 0;
+  // scale factors: 16 columns per operand (4 K-chunks x 4 columns), the K
+  // ones per K stage
+  static constexpr uint32_t kTmemSfa = 384;
+  static constexpr uint32_t kTmemSfb = 400;
+};
+
+template <bool FP4Q>
+struct Layout {
+  using P = Plan<FP4Q>;
+  static constexpr int kRawStageBytes = kBlockPages * P::kRawPageBytes;
+  static constexpr int kVBytes = 256 * kBlockKeys * 2;   // fp16 V^T [256 dims][64 keys]
+  static constexpr int kPBytes = 128 * kBlockKeys * 2;   // fp16 P [128 rows][64 keys]
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + P::kKStages * P::kKBytes;
+  static constexpr int kPOff = kVOff + P::kVStages * kVBytes;
+  static constexpr int kRawOff = kPOff + P::kPStages * kPBytes;
+  static constexpr int kQOff = kRawOff + P::kRawStages * kRawStageBytes;  // FP4 Q codes
+  static constexpr int kSfaXOff = kQOff + P::kQBytes;
+  static constexpr int kScrOff = kSfaXOff + P::kSfaXBytes;  // per dequant warp: V scales
+  static constexpr int kScrWarpBytes = kBlockPages * 32;   // [page][2 blocks][16 slots]
+  static constexpr int kBarOff = kScrOff + kDequantWarps * kScrWarpBytes;
+  // barriers, in this order
+  static constexpr int B_RAW_FULL = 0;
+  static constexpr int B_RAW_EMPTY = B_RAW_FULL + P::kRawStages;
+  static constexpr int B_K_FULL = B_RAW_EMPTY + P::kRawStages;
+  static constexpr int B_K_FREE = B_K_FULL + P::kKStages;
+  static constexpr int B_KC_FULL = B_K_FREE + P::kKStages;  // FP4: K codes landed (TMA bytes)
+  static constexpr int B_V_FULL = B_KC_FULL + P::kKStages;
+  static constexpr int B_V_FREE = B_V_FULL + P::kVStages;
+  static constexpr int B_S_FULL = B_V_FREE + P::kVStages;
+  static constexpr int B_S_FREE = B_S_FULL + P::kSStages;
+  static constexpr int B_P_FULL = B_S_FREE + P::kSStages;
+  static constexpr int B_PV_DONE = B_P_FULL + P::kPStages;
+  static constexpr int B_Q_FULL = B_PV_DONE + P::kPStages;
+  static constexpr int B_FINAL = B_Q_FULL + 1;
+  static constexpr int kNumBars = B_FINAL + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, raw valid[]
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+  static_assert(kSmemBytes <= 232448, "prefill shared memory plan too large");
+  static_assert(kQOff % 1024 == 0 && P::kKBytes % 1024 == 0 && P::kRawPageBytes % 1024 == 0,
+                "128-byte-swizzled tiles need 1,024-byte alignment");
+  static_assert(P::kRawStages >= 2 && P::kRawStages <= 8, "raw valid words live in misc[2 .. 9]");
+  // TMEM: the S ring at 0 and 64, O at 128 .. 383, then Q (fp16) or the scale factors
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemS = 0;
+  static constexpr uint32_t kTmemO = P::kSStages * kBlockKeys;
+  static_assert(kTmemO + 256 <= 384, "TMEM plan: S ring and O");
+  static_assert(FP4Q ? P::kTmemSfb + 16 * P::kKStages <= kTmemCols : P::kTmemQ + 128 <= kTmemCols,
+                "TMEM plan too large");
+};
 
 struct PrefillArgs {
   int64_t num_pages;
   int32_t hkv, group, tpt;  // tpt: query tokens per tile (128 / group)
   float qk_scale_log2, out_scale;
+  float q_scale, q_enc;     // FP4 queries: decode scale g_Q and fp32(1 / (6 g_Q))
   const uint16_t* q;
   const int32_t* qo_indptr;
   const int32_t* page_table;
   int64_t pt_stride;
   const int32_t* seq_lens;
   int32_t batch, hq, max_qlen, rows_per_slot, causal;
-  int32_t splits;  // key-range splits per tile (slots per (sequence, KV head))
+  int64_t total_q;  // rows of q (qo_indptr[batch] must not exceed it)
+  int32_t splits;   // key-range splits per tile (slots per (sequence, KV head))
+  uint64_t wait_ns; // bound of a pipeline wait
   float* o_part;
   float* lse_part;
   int64_t part_slots;
@@ -145,9 +199,28 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// Same for a K-major tile of 128-byte rows written with 128-byte swizzling
+// (8-row atoms of 1,024 bytes, 1,024-byte aligned): the stride between 8-row
+// groups is 1,024 bytes, the leading offset is unused, and the start address
+// advances along K inside the 128-byte row (32 bytes per FP4 K-chunk).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format 1), E4M3
+// scale factors (format bit 0), both K-major, dense K 64, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -166,6 +239,18 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
           d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Block-scaled FP4 product: D (+)= (A x SFA) (B x SFB), K 64, one E4M3 scale
+// per 16 elements along K taken from TMEM (four per row per instruction).
+__device__ __forceinline__ void umma_fp4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0;"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 
@@ -209,6 +294,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Scale factors of a block-scaled operand in TMEM: for one K-chunk of 64
+// elements (four 16-element blocks) the scale bytes of up to 128 operand rows
+// take 4 columns, row r's four bytes (blocks in byte order) in column r / 32
+// of lane r % 32, repeated in every 32-lane quarter so that each quarter's
+// datapath finds them in its own lanes.  This warp's lane l writes the 16
+// columns of K-chunks 0 .. 3 at taddr (its own lane): column 4c + j = word(l
+// + 32 j, c), the scale word of row l + 32 j and chunk c.
+template <typename F>
+__device__ __forceinline__ void store_scale_factors(uint32_t taddr, int l, F word) {
+  uint32_t r[16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[4 * c + j] = word(l + 32 * j, c);
+  tmem_st16(taddr, r);
+}
+
 // --------------------------------------------------------------- tiles --
 // Work items enumerate (sequence, KV head, token tile, key split); every role
 // of a CTA walks the same list: item = blockIdx.x + k * gridDim.x.  When
@@ -224,12 +326,21 @@ struct Tile {
   int keys;          // keys the last row of the tile may see
 };
 
+// Error bits of a sequence's row range and length (0 when both are valid).
+__device__ __forceinline__ int seq_errors(const PrefillArgs& a, int q0, int qlen, int len) {
+  int e = 0;
+  if (qlen < 0 || qlen > a.max_qlen || qlen > len || q0 < 0 || static_cast<int64_t>(q0) + qlen > a.total_q)
+    e |= PNKV_DEV_ERR_QO_INDPTR;
+  if (len < 0 || static_cast<int64_t>((len + 15) >> 4) > a.pt_stride) e |= PNKV_DEV_ERR_SEQ_LEN;
+  return e;
+}
+
+// Sequence b has query rows and valid geometry.
 __device__ __forceinline__ bool seq_ok(const PrefillArgs& a, int b, int* q0, int* qlen, int* len) {
   *len = __ldg(a.seq_lens + b);
   *q0 = __ldg(a.qo_indptr + b);
   *qlen = __ldg(a.qo_indptr + b + 1) - *q0;
-  return *qlen > 0 && *qlen <= a.max_qlen && *qlen <= *len && *q0 >= 0 &&
-         static_cast<int64_t>((*len + 15) >> 4) <= a.pt_stride;
+  return *qlen > 0 && seq_errors(a, *q0, *qlen, *len) == 0;
 }
 
 // The idx-th tile, or false if there is none.
@@ -267,52 +378,68 @@ __device__ bool find_tile(const PrefillArgs& a, int64_t idx, Tile* t) {
 // Parity of the phase in which item g of a ring of n slots lands in its slot.
 __device__ __forceinline__ uint32_t ring_parity(int64_t g, int n) { return static_cast<uint32_t>((g / n) & 1); }
 
+template <bool FP4Q>
 __device__ __forceinline__ uint64_t* bar_at(uint8_t* smem, int i) {
-  return reinterpret_cast<uint64_t*>(smem + kBarOff) + i;
+  return reinterpret_cast<uint64_t*>(smem + Layout<FP4Q>::kBarOff) + i;
 }
+
+// tmap: the pool as 128-byte rows with a box of Plan::kRawRows rows (whole
+// records for the fp16 variant, the 20 rows after the K codes for the FP4
+// one); tmap_k (FP4 only): the same rows with a box of the 16 K-code rows.
+template <bool FP4Q>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillArgs a) {
+    prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_k,
+                        const PrefillArgs a) {
+  using P = Plan<FP4Q>;
+  using L = Layout<FP4Q>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* abort_flag = misc + 1;
   uint32_t* raw_valid = misc + 2;  // [kRawStages] bit p: page p of the block loaded
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return bar_at<FP4Q>(smem, i); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRawStages; ++i) {
-      mbar_init(bar_at(smem, B_RAW_FULL + i), 1);
-      mbar_init(bar_at(smem, B_RAW_EMPTY + i), kDequantWarps);
+    for (int i = 0; i < P::kRawStages; ++i) {
+      mbar_init(bar(L::B_RAW_FULL + i), 1);
+      mbar_init(bar(L::B_RAW_EMPTY + i), kDequantWarps);
     }
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(bar_at(smem, B_K_FULL + i), kDequantWarps);
-      mbar_init(bar_at(smem, B_K_FREE + i), 1);
+    for (int i = 0; i < P::kKStages; ++i) {
+      // fp16: the dequant warps (K widened); FP4: the four warps that write
+      // the K scale factors, with the codes' bytes counted on B_KC_FULL
+      mbar_init(bar(L::B_K_FULL + i), FP4Q ? 4 : kDequantWarps);
+      mbar_init(bar(L::B_K_FREE + i), 1);
+      mbar_init(bar(L::B_KC_FULL + i), 1);
     }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(bar_at(smem, B_V_FULL + i), kDequantWarps);
-      mbar_init(bar_at(smem, B_V_FREE + i), 1);
+    for (int i = 0; i < P::kVStages; ++i) {
+      mbar_init(bar(L::B_V_FULL + i), kDequantWarps);
+      mbar_init(bar(L::B_V_FREE + i), 1);
     }
-    for (int i = 0; i < kSStages; ++i) {
-      mbar_init(bar_at(smem, B_S_FULL + i), 1);
-      mbar_init(bar_at(smem, B_S_FREE + i), 4);
+    for (int i = 0; i < P::kSStages; ++i) {
+      mbar_init(bar(L::B_S_FULL + i), 1);
+      mbar_init(bar(L::B_S_FREE + i), 4);
     }
-    for (int i = 0; i < kPStages; ++i) {
-      mbar_init(bar_at(smem, B_P_FULL + i), 4);
-      mbar_init(bar_at(smem, B_PV_DONE + i), 1);
+    for (int i = 0; i < P::kPStages; ++i) {
+      mbar_init(bar(L::B_P_FULL + i), 4);
+      mbar_init(bar(L::B_PV_DONE + i), 1);
     }
-    mbar_init(bar_at(smem, B_Q_FULL), 4);
-    mbar_init(bar_at(smem, B_FINAL), 2);  // one arrival per MMA-issuing thread
+    mbar_init(bar(L::B_Q_FULL), 4);
+    mbar_init(bar(L::B_FINAL), 2);  // one arrival per MMA-issuing thread
     *abort_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(misc)),
-                 "r"(kTmemCols)
+                 "r"(L::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
-  if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap);
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap);
+    if (FP4Q) tma_prefetch_desc(&tmap_k);
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
@@ -325,10 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // single-thread wait (the MMA issuer, producer lane 0); a completed phase
   // returns at once, without reading the abort flag
-  auto wait = [&](int bar, uint32_t parity) -> bool {
-    if (mbar_try_wait(bar_at(smem, bar), parity)) return true;
+  auto wait = [&](int b, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar(b), parity)) return true;
     if (*abort_flag) return false;
-    if (!mbar_wait(bar_at(smem, bar), parity)) {
+    if (!mbar_wait(bar(b), parity, a.wait_ns)) {
       fail();
       return false;
     }
@@ -336,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // warp-uniform wait: every lane waits, the warp agrees on the outcome, so
   // an abort never splits a warp before a collective operation
-  auto wait_warp = [&](int bar, uint32_t parity) -> bool {
-    bool ok = !*abort_flag && mbar_wait(bar_at(smem, bar), parity);
+  auto wait_warp = [&](int b, uint32_t parity) -> bool {
+    bool ok = !*abort_flag && mbar_wait(bar(b), parity, a.wait_ns);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && lane == 0) fail();
     return ok;
@@ -353,17 +480,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* row = a.page_table + static_cast<int64_t>(t.b) * a.pt_stride;
       const int pages = (t.len + 15) >> 4;
       for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
-        const int rs = static_cast<int>(gb % kRawStages);
-        if (lane == 0) ok = wait(B_RAW_EMPTY + rs, ring_parity(gb, kRawStages) ^ 1u);
+        const int rs = static_cast<int>(gb % P::kRawStages);
+        const int ks = static_cast<int>(gb % P::kKStages);
+        if (lane == 0) {
+          ok = wait(L::B_RAW_EMPTY + rs, ring_parity(gb, P::kRawStages) ^ 1u);
+          // FP4: the K-code slot is free once the QK of block gb - kKStages completed
+          if (FP4Q && ok && gb >= P::kKStages) ok = wait(L::B_K_FREE + ks, ring_parity(gb - P::kKStages, P::kKStages));
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         // lanes 0 .. kBlockPages - 1: the block's pages
         int32_t page = -1;
-        bool in_seq = false;
         if (lane < kBlockPages) {
           const int pi = kBlockPages * (t.kb0 + j) + lane;
-          in_seq = pi < pages;
-          if (in_seq) {
+          if (pi < pages) {
             page = __ldg(row + pi);
             if (page < 0 || page >= a.num_pages) {
               flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
@@ -374,21 +504,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned load = __ballot_sync(0xffffffffu, lane < kBlockPages && page >= 0);
         if (lane == 0) {
           raw_valid[rs] = load;
-          mbar_arrive_expect_tx(bar_at(smem, B_RAW_FULL + rs), __popc(load) * kRecBytes);
+          mbar_arrive_expect_tx(bar(L::B_RAW_FULL + rs), __popc(load) * P::kRawTx);
+          if (FP4Q) mbar_arrive_expect_tx(bar(L::B_KC_FULL + ks), __popc(load) * (16 * 128));
         }
         __syncwarp();
         if (lane < kBlockPages && page >= 0) {
           const int32_t y = (page * a.hkv + t.h) * 36;
-          tma_load_2d(smem + kRawOff + rs * kRawStageBytes + lane * kRawPageBytes, &tmap, 0, y,
-                      bar_at(smem, B_RAW_FULL + rs), policy);
+          tma_load_2d(smem + L::kRawOff + rs * L::kRawStageBytes + lane * P::kRawPageBytes, &tmap, 0,
+                      y + P::kRawRow0, bar(L::B_RAW_FULL + rs), policy);
+          if (FP4Q)
+            tma_load_2d(smem + L::kKOff + ks * P::kKBytes + lane * (16 * 128), &tmap_k, 0, y,
+                        bar(L::B_KC_FULL + ks), policy);
         }
       }
     }
     if (!ok && lane == 0) {
-      // bounded drain of the loads that may still be landing
-      const int64_t first = gb > kRawStages ? gb - kRawStages : 0;
+      // drain of the loads that may still be landing (fixed bound: a CTA must
+      // not exit with a bulk copy in flight); every block below gb was armed
+      const int64_t first = gb > P::kRawStages ? gb - P::kRawStages : 0;
       for (int64_t i = first; i < gb; ++i)
-        mbar_wait(bar_at(smem, B_RAW_FULL + static_cast<int>(i % kRawStages)), ring_parity(i, kRawStages));
+        mbar_wait(bar(L::B_RAW_FULL + static_cast<int>(i % P::kRawStages)), ring_parity(i, P::kRawStages));
+      if (FP4Q) {
+        const int64_t fk = gb > P::kKStages ? gb - P::kKStages : 0;
+        for (int64_t i = fk; i < gb; ++i)
+          mbar_wait(bar(L::B_KC_FULL + static_cast<int>(i % P::kKStages)), ring_parity(i, P::kKStages));
+      }
     }
   } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
     // ----------------------------------------------------------- dequant
@@ -398,83 +538,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tile t;
     for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x) {
       for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
-        const int rs = static_cast<int>(gb % kRawStages);
-        const int ks = static_cast<int>(gb % kKStages), vs = static_cast<int>(gb % kVStages);
-        ok = wait_warp(B_RAW_FULL + rs, ring_parity(gb, kRawStages));
+        const int rs = static_cast<int>(gb % P::kRawStages);
+        const int ks = static_cast<int>(gb % P::kKStages), vs = static_cast<int>(gb % P::kVStages);
+        ok = wait_warp(L::B_RAW_FULL + rs, ring_parity(gb, P::kRawStages));
         // K slot: free once the QK of block gb - kKStages completed
-        if (ok && gb >= kKStages) ok = wait_warp(B_K_FREE + ks, ring_parity(gb - kKStages, kKStages));
+        if (ok && gb >= P::kKStages && (!FP4Q || warp < kDequantWarp0 + 4))
+          ok = wait_warp(L::B_K_FREE + ks, ring_parity(gb - P::kKStages, P::kKStages));
         if (!ok) break;
         const uint32_t valid = raw_valid[rs];
-        const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStageBytes);
-        uint8_t* ktile = smem + kKOff + ks * kKBytes;
-        uint8_t* vtile = smem + kVOff + vs * kVBytes;
-        // K: 1,024 units (key, 16-dim block); the lanes of a warp take 32
-        // consecutive keys, so each quarter-warp stores one contiguous
-        // 128-byte core matrix (8 keys x 8 dims)
-        static_assert(kDequantWarps * 32 == 256, "unit mapping assumes 256 dequant threads");
-        // all loads first: a load may not pass an earlier shared-memory store
-        uint2 kw[4];
-        uint32_t ksb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int key = (dt & 31) + 32 * (i & 1), blk = (dt >> 5) + 8 * (i >> 1);
-          const int pg = key >> 4, slot = key & 15;
-          kw[i] = make_uint2(0, 0);
-          ksb[i] = 0;
-          if ((valid >> pg) & 1) {
-            const uint32_t rec = raw + pg * kRawPageBytes;
-            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(kw[i].x), "=r"(kw[i].y) : "r"(rec + swz128(slot, 8 * blk)));
-            ksb[i] = lds8(rec + swz128(16 + (slot >> 3), (slot & 7) * 16 + blk));
+        const uint32_t raw = smem_addr(smem + L::kRawOff + rs * L::kRawStageBytes);
+        if constexpr (FP4Q) {
+          // the K scales of the block's 64 keys as the B operand's scale
+          // factors, one copy per TMEM lane quarter (warps 4-7 hold quarters
+          // 0-3); key n = page n / 16, slot n % 16, whose 16 scale bytes are
+          // raw row slot / 8 (record row 16 + slot / 8), bytes 16 (slot % 8) ..
+          if (warp < kDequantWarp0 + 4) {
+            const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + P::kTmemSfb + ks * 16;
+            store_scale_factors(taddr, lane, [&](int n, int c) -> uint32_t {
+              if (n >= kBlockKeys) return 0u;
+              const int pg = n >> 4, slot = n & 15;
+              if (!((valid >> pg) & 1)) return 0u;  // a missing page scales to zero
+              return lds32(raw + pg * P::kRawPageBytes + swz128(slot >> 3, (slot & 7) * 16 + 4 * c));
+            });
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::B_K_FULL + ks));
           }
-        }
+        } else {
+          uint8_t* ktile = smem + L::kKOff + ks * P::kKBytes;
+          // K: 1,024 units (key, 16-dim block); the lanes of a warp take 32
+          // consecutive keys, so each quarter-warp stores one contiguous
+          // 128-byte core matrix (8 keys x 8 dims)
+          static_assert(kDequantWarps * 32 == 256, "unit mapping assumes 256 dequant threads");
+          // all loads first: a load may not pass an earlier shared-memory store
+          uint2 kw[4];
+          uint32_t ksb[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int key = (dt & 31) + 32 * (i & 1), blk = (dt >> 5) + 8 * (i >> 1);
-          // a missing page has zero codes and a zero scale: fp16 zeros
-          uint32_t s2 = e4m3x2_to_f16x2(ksb[i]);
-          s2 = prmt(s2, s2, 0x1010u);
-          uint32_t c0[4], c1[4];
-          e2m1x8_unpack(kw[i].x, c0);
-          e2m1x8_unpack(kw[i].y, c1);
-          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk, 256)) =
-              make_uint4(hmul2(c0[0], s2), hmul2(c0[1], s2), hmul2(c0[2], s2), hmul2(c0[3], s2));
-          *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk + 8, 256)) =
-              make_uint4(hmul2(c1[0], s2), hmul2(c1[1], s2), hmul2(c1[2], s2), hmul2(c1[3], s2));
+          for (int i = 0; i < 4; ++i) {
+            const int key = (dt & 31) + 32 * (i & 1), blk = (dt >> 5) + 8 * (i >> 1);
+            const int pg = key >> 4, slot = key & 15;
+            kw[i] = make_uint2(0, 0);
+            ksb[i] = 0;
+            if ((valid >> pg) & 1) {
+              const uint32_t rec = raw + pg * P::kRawPageBytes;
+              asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(kw[i].x), "=r"(kw[i].y) : "r"(rec + swz128(slot, 8 * blk)));
+              ksb[i] = lds8(rec + swz128(16 + (slot >> 3), (slot & 7) * 16 + blk));
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int key = (dt & 31) + 32 * (i & 1), blk = (dt >> 5) + 8 * (i >> 1);
+            // a missing page has zero codes and a zero scale: fp16 zeros
+            uint32_t s2 = e4m3x2_to_f16x2(ksb[i]);
+            s2 = prmt(s2, s2, 0x1010u);
+            uint32_t c0[4], c1[4];
+            e2m1x8_unpack(kw[i].x, c0);
+            e2m1x8_unpack(kw[i].y, c1);
+            *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk, 256)) =
+                make_uint4(hmul2(c0[0], s2), hmul2(c0[1], s2), hmul2(c0[2], s2), hmul2(c0[3], s2));
+            *reinterpret_cast<uint4*>(ktile + core_off(key, 16 * blk + 8, 256)) =
+                make_uint4(hmul2(c1[0], s2), hmul2(c1[1], s2), hmul2(c1[2], s2), hmul2(c1[3], s2));
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::B_K_FULL + ks));
         }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(smem, B_K_FULL + ks));
         // V slot: free once the P V of block gb - kVStages completed
-        if (gb >= kVStages) ok = wait_warp(B_V_FREE + vs, ring_parity(gb - kVStages, kVStages));
+        if (gb >= P::kVStages) ok = wait_warp(L::B_V_FREE + vs, ring_parity(gb - P::kVStages, P::kVStages));
         if (!ok) break;
+        uint8_t* vtile = smem + L::kVOff + vs * L::kVBytes;
         // V^T: thread dt owns dim d = dt over the block's 64 keys.  The
         // lanes of a warp read consecutive code bytes of a slot-pair row, and
         // each quarter-warp stores one contiguous core matrix (8 dims x 8
         // keys).  The block scales of the warp's two 16-dim blocks are first
         // transposed through a per-warp scratch ([page][block][slot]), so a
         // thread reads the 16 slot scales of its block with one 16-byte load.
+        // (Raw rows are record rows minus kRawRow0: V codes at record rows
+        // 18 .. 33, V scales at 34 and 35.)
         {
           const int d = dt;
           const int wq = dt >> 5;
-          const uint32_t scr = smem_addr(smem + kScrOff + wq * kScrWarpBytes);
+          const uint32_t scr = smem_addr(smem + L::kScrOff + wq * L::kScrWarpBytes);
           {
             const int slot = lane & 15, bsel = lane >> 4, blk = 2 * wq + bsel;
 #pragma unroll
             for (int pg = 0; pg < kBlockPages; ++pg) {
-              const uint32_t b = ((valid >> pg) & 1)
-                                     ? lds8(raw + pg * kRawPageBytes + swz128(34 + (slot >> 3), (slot & 7) * 16 + blk))
-                                     : 0u;
+              const uint32_t b = ((valid >> pg) & 1) ? lds8(raw + pg * P::kRawPageBytes +
+                                                            swz128(34 - P::kRawRow0 + (slot >> 3), (slot & 7) * 16 + blk))
+                                                     : 0u;
               asm volatile("st.shared.u8 [%0], %1;" ::"r"(scr + pg * 32 + bsel * 16 + slot), "h"(static_cast<uint16_t>(b)));
             }
           }
           __syncwarp();
-          const uint32_t code_row = 18 + (d >> 7), code_col = d & 127;
+          const uint32_t code_row = 18 - P::kRawRow0 + (d >> 7), code_col = d & 127;
           // all loads first (codes of the four pages, then their scales)
           uint32_t code[kBlockPages][8];
           uint4 sc[kBlockPages];
 #pragma unroll
           for (int pg = 0; pg < kBlockPages; ++pg) {
-            const uint32_t rec = raw + pg * kRawPageBytes;
+            const uint32_t rec = raw + pg * P::kRawPageBytes;
 #pragma unroll
             for (int pr = 0; pr < 8; ++pr) code[pg][pr] = lds8(rec + swz128(code_row + 2 * pr, code_col));
             sc[pg] = lds128(scr + pg * 32 + ((d >> 4) & 1) * 16);
@@ -497,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar_at(smem, B_V_FULL + vs));
-          mbar_arrive(bar_at(smem, B_RAW_EMPTY + rs));
+          mbar_arrive(bar(L::B_V_FULL + vs));
+          mbar_arrive(bar(L::B_RAW_EMPTY + rs));
         }
       }
     }
@@ -510,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // never stall the P V stream and the other way round.
     if (lane == 0) {
       const bool qk_role = warp == kQkWarp;
-      const uint32_t idesc = qk_role ? idesc_f16(128, kBlockKeys) : idesc_f16(128, 256);
+      const uint32_t idesc = qk_role ? (FP4Q ? idesc_mxf4nvf4(128, kBlockKeys) : idesc_f16(128, kBlockKeys))
+                                     : idesc_f16(128, 256);
       int64_t gb = 0;  // first block of the current tile
       int64_t tcount = 0;
       bool ok = true, issued_any = false;
@@ -518,50 +682,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x, ++tcount) {
         const int64_t g0 = gb;
         if (qk_role) {
-          // Q of this tile is in TMEM (written by the softmax warps)
-          ok = wait(B_Q_FULL, static_cast<uint32_t>(tcount & 1));
+          // Q of this tile is ready (fp16 in TMEM, or FP4 codes in shared
+          // memory with their scale factors in TMEM), written by the softmax warps
+          ok = wait(L::B_Q_FULL, static_cast<uint32_t>(tcount & 1));
           for (int j = 0; ok && j < t.nblocks; ++j) {
             const int64_t g = g0 + j;
-            const int ks = static_cast<int>(g % kKStages), ss = static_cast<int>(g % kSStages);
-            ok = wait(B_K_FULL + ks, ring_parity(g, kKStages)) &&
-                 (g < kSStages || wait(B_S_FREE + ss, ring_parity(g - kSStages, kSStages)));
+            const int ks = static_cast<int>(g % P::kKStages), ss = static_cast<int>(g % P::kSStages);
+            ok = wait(L::B_K_FULL + ks, ring_parity(g, P::kKStages)) &&
+                 (!FP4Q || wait(L::B_KC_FULL + ks, ring_parity(g, P::kKStages))) &&
+                 (g < P::kSStages || wait(L::B_S_FREE + ss, ring_parity(g - P::kSStages, P::kSStages)));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t k_base = smem_addr(smem + kKOff + ks * kKBytes);
+            const uint32_t k_base = smem_addr(smem + L::kKOff + ks * P::kKBytes);
+            if constexpr (FP4Q) {
+              const uint32_t q_base = smem_addr(smem + L::kQOff);
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk)  // 16 dims = 8 TMEM columns of Q per k-step
-              umma_f16_ta(tmem + kTmemS + ss * kBlockKeys, tmem + kTmemQ + kk * 8,
-                          smem_desc(k_base + kk * 256, 128, 4096), idesc, kk > 0);
-            umma_commit(bar_at(smem, B_S_FULL + ss));
-            umma_commit(bar_at(smem, B_K_FREE + ks));
+              for (int c = 0; c < 4; ++c)  // 64 FP4 elements = 32 bytes of every row per K-chunk
+                umma_fp4(tmem + L::kTmemS + ss * kBlockKeys, smem_desc_sw128(q_base + 32 * c),
+                         smem_desc_sw128(k_base + 32 * c), idesc, tmem + P::kTmemSfa + 4 * c,
+                         tmem + P::kTmemSfb + ks * 16 + 4 * c, c > 0);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 16; ++kk)  // 16 dims = 8 TMEM columns of Q per k-step
+                umma_f16_ta(tmem + L::kTmemS + ss * kBlockKeys, tmem + P::kTmemQ + kk * 8,
+                            smem_desc(k_base + kk * 256, 128, 4096), idesc, kk > 0);
+            }
+            umma_commit(bar(L::B_S_FULL + ss));
+            umma_commit(bar(L::B_K_FREE + ks));
             issued_any = true;
           }
         } else {
           for (int j = 0; ok && j < t.nblocks; ++j) {
             const int64_t g = g0 + j;
-            const int ps = static_cast<int>(g % kPStages), vs = static_cast<int>(g % kVStages);
-            ok = wait(B_P_FULL + ps, ring_parity(g, kPStages)) && wait(B_V_FULL + vs, ring_parity(g, kVStages));
+            const int ps = static_cast<int>(g % P::kPStages), vs = static_cast<int>(g % P::kVStages);
+            ok = wait(L::B_P_FULL + ps, ring_parity(g, P::kPStages)) &&
+                 wait(L::B_V_FULL + vs, ring_parity(g, P::kVStages));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t p_base = smem_addr(smem + kPOff + ps * kPBytes);
-            const uint32_t v_base = smem_addr(smem + kVOff + vs * kVBytes);
+            const uint32_t p_base = smem_addr(smem + L::kPOff + ps * L::kPBytes);
+            const uint32_t v_base = smem_addr(smem + L::kVOff + vs * L::kVBytes);
 #pragma unroll
             for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-              umma_f16(tmem + kTmemO, smem_desc(p_base + kk * 256, 128, kBlockKeys * 16),
+              umma_f16(tmem + L::kTmemO, smem_desc(p_base + kk * 256, 128, kBlockKeys * 16),
                        smem_desc(v_base + kk * 256, 128, kBlockKeys * 16), idesc, (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(bar_at(smem, B_V_FREE + vs));
-            umma_commit(bar_at(smem, B_PV_DONE + ps));
+            umma_commit(bar(L::B_V_FREE + vs));
+            umma_commit(bar(L::B_PV_DONE + ps));
             issued_any = true;
           }
         }
         gb = g0 + t.nblocks;
       }
-      // every issued MMA completes before TMEM is released
+      // every issued MMA completes before TMEM is released (fixed bound)
       if (issued_any)
-        umma_commit(bar_at(smem, B_FINAL));
+        umma_commit(bar(L::B_FINAL));
       else
-        mbar_arrive(bar_at(smem, B_FINAL));
-      mbar_wait(bar_at(smem, B_FINAL), 0);
+        mbar_arrive(bar(L::B_FINAL));
+      mbar_wait(bar(L::B_FINAL), 0);
     }
     __syncwarp();
   } else {
@@ -577,46 +753,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = r % a.group;
       const bool row_live = r < a.tpt * a.group && r / a.group < t.ntok;
       const int lim = !row_live ? 0 : (a.causal ? t.len - t.qlen + tok + 1 : t.len);
-      // Q row -> fp16 into this thread's TMEM lane (the previous tile's MMAs
-      // are done: its epilogue waited for the last P V)
+      // the four softmax warps enter a tile together, so each arrives on
+      // B_Q_FULL once per tile even when tiles without key blocks follow
+      // each other (and the FP4 scale exchange below is not overwritten
+      // while another warp still reads it)
+      named_bar_sync(1, 128);
+      // Q row into its operand (the previous tile's MMAs are done: its
+      // epilogue waited for the last P V, and every QK before that was read)
       {
         const uint4* src = row_live ? reinterpret_cast<const uint4*>(
                                           a.q + (static_cast<int64_t>(t.q0 + tok) * a.hq + t.h * a.group + head) * 256)
                                     : nullptr;
+        if constexpr (FP4Q) {
+          // NVFP4 codes of the row (the cache's encoder, decode scale g_Q)
+          // into row r of the 128-byte-swizzled A tile; the 16 scale bytes
+          // through shared memory into the A scale factors in TMEM
+          uint8_t* qt = smem + L::kQOff + r * 128;
+          uint32_t* sfx = reinterpret_cast<uint32_t*>(smem + L::kSfaXOff);  // [128 rows][4 words]
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {  // 32 dims = 16 columns per store
-          uint32_t h[16];
+          for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch: blocks 2ch, 2ch + 1
+            uint32_t cw[4];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_live) w = __ldg(src + 4 * c + v);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int hb = 0; hb < 2; ++hb) {
+              const int blk = 2 * ch + hb;
+              float x[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              h[4 * v + e] = f32x2_to_f16x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xFFFF0000u));
+              for (int v = 0; v < 2; ++v) {
+                uint4 w = make_uint4(0, 0, 0, 0);
+                if (row_live) w = __ldg(src + 2 * blk + v);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  x[8 * v + 2 * e] = __uint_as_float(ws[e] << 16);
+                  x[8 * v + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
+                }
+              }
+              float amax = 0.f;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(x[e]));
+              float rcp;
+              const uint32_t sb = nvfp4_block_scale(amax, a.q_scale, a.q_enc, &rcp);
+              uint32_t lo = 0u, hi = 0u;
+              if (sb != 0u) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  lo |= e2m1_code(__fmul_rn(x[e], rcp)) << (4 * e);
+                  hi |= e2m1_code(__fmul_rn(x[8 + e], rcp)) << (4 * e);
+                }
+              }
+              cw[2 * hb] = lo;
+              cw[2 * hb + 1] = hi;
+              // scale byte of block blk: byte blk % 4 of word blk / 4
+              reinterpret_cast<uint8_t*>(sfx + 4 * r)[blk] = static_cast<uint8_t>(sb);
+            }
+            *reinterpret_cast<uint4*>(qt + ((ch ^ (r & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
           }
-          tmem_st16(lane_addr + kTmemQ + 16 * c, h);
+          named_bar_sync(1, 128);
+          store_scale_factors(lane_addr + P::kTmemSfa, lane,
+                              [&](int n, int c) -> uint32_t { return sfx[4 * n + c]; });
+          fence_proxy_async();  // the A tile's generic stores, before the MMA reads them
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {  // 32 dims = 16 columns per store
+            uint32_t h[16];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w = make_uint4(0, 0, 0, 0);
+              if (row_live) w = __ldg(src + 4 * c + v);
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                h[4 * v + e] = f32x2_to_f16x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xFFFF0000u));
+            }
+            tmem_st16(lane_addr + P::kTmemQ + 16 * c, h);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(smem, B_Q_FULL));
+        if (lane == 0) mbar_arrive(bar(L::B_Q_FULL));
       }
       float m_used = -INFINITY, l = 0.f;
       const int64_t g0 = gb;
       for (int j = 0; j < t.nblocks; ++j) {
         const int64_t g = g0 + j;
-        const int ss = static_cast<int>(g % kSStages), ps = static_cast<int>(g % kPStages);
-        ok = wait_warp(B_S_FULL + ss, ring_parity(g, kSStages));
+        const int ss = static_cast<int>(g % P::kSStages), ps = static_cast<int>(g % P::kPStages);
+        ok = wait_warp(L::B_S_FULL + ss, ring_parity(g, P::kSStages));
         if (!ok) break;
         tc_fence_after();
         uint32_t sr[kBlockKeys];
-        tmem_ld32(lane_addr + kTmemS + ss * kBlockKeys, sr);
-        tmem_ld32(lane_addr + kTmemS + ss * kBlockKeys + 32, sr + 32);
+        tmem_ld32(lane_addr + L::kTmemS + ss * kBlockKeys, sr);
+        tmem_ld32(lane_addr + L::kTmemS + ss * kBlockKeys + 32, sr + 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(smem, B_S_FREE + ss));
+        if (lane == 0) mbar_arrive(bar(L::B_S_FREE + ss));
         // the row maximum of the raw logits over the visible keys (masked
         // keys become -inf); the logit scale is positive, so the maximum of
         // the scaled logits is the scaled maximum
@@ -642,18 +873,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O holds this row's sum so far only after at least one P V
         const bool need = move && m_used != -INFINITY && j > 0;
         if (__any_sync(0xffffffffu, need)) {
-          ok = wait_warp(B_PV_DONE + static_cast<int>((g - 1) % kPStages), ring_parity(g - 1, kPStages));
+          ok = wait_warp(L::B_PV_DONE + static_cast<int>((g - 1) % P::kPStages), ring_parity(g - 1, P::kPStages));
           if (!ok) break;
           tc_fence_after();
           const float f = need ? alpha : 1.f;
 #pragma unroll 1
           for (int c = 0; c < 256; c += 16) {
             uint32_t x[16];
-            tmem_ld16(lane_addr + kTmemO + c, x);
+            tmem_ld16(lane_addr + L::kTmemO + c, x);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * f);
-            tmem_st16(lane_addr + kTmemO + c, x);
+            tmem_st16(lane_addr + L::kTmemO + c, x);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -675,18 +906,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l += add0 + add1;
         // P slot ps was last read by the P V of block g - kPStages
-        if (g >= kPStages) {
-          ok = wait_warp(B_PV_DONE + ps, ring_parity(g - kPStages, kPStages));
+        if (g >= P::kPStages) {
+          ok = wait_warp(L::B_PV_DONE + ps, ring_parity(g - P::kPStages, P::kPStages));
           if (!ok) break;
         }
-        uint8_t* pt = smem + kPOff + ps * kPBytes;
+        uint8_t* pt = smem + L::kPOff + ps * L::kPBytes;
 #pragma unroll
         for (int c = 0; c < kBlockKeys / 8; ++c)
           *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
               make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(smem, B_P_FULL + ps));
+        if (lane == 0) mbar_arrive(bar(L::B_P_FULL + ps));
       }
       if (!ok) break;
       gb = g0 + t.nblocks;
@@ -694,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // split) slot (an item with no key block writes zeros and LSE -inf)
       if (t.nblocks > 0) {
         const int64_t gl = gb - 1;
-        ok = wait_warp(B_PV_DONE + static_cast<int>(gl % kPStages), ring_parity(gl, kPStages));
+        ok = wait_warp(L::B_PV_DONE + static_cast<int>(gl % P::kPStages), ring_parity(gl, P::kPStages));
         if (!ok) break;
         tc_fence_after();
       }
@@ -708,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 256; c += 16) {
         uint32_t x[16];
-        tmem_ld16(lane_addr + kTmemO + c, x);
+        tmem_ld16(lane_addr + L::kTmemO + c, x);
         tmem_wait_ld();
         if (write) {
 #pragma unroll
@@ -731,11 +962,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::kTmemCols) : "memory");
   }
 }
 
-// Work metadata header and empty segments (sequences without query rows).
+// Work metadata header and empty segments (sequences without query rows, or
+// flagged ones).
 __global__ void prefill_meta_kernel(const PrefillArgs a) {
   griddep_wait();
   griddep_launch_dependents();
@@ -748,8 +980,8 @@ __global__ void prefill_meta_kernel(const PrefillArgs a) {
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.batch; b += gridDim.x * blockDim.x) {
     int q0, qlen, len;
     if (!seq_ok(a, b, &q0, &qlen, &len)) {
-      if (__ldg(a.qo_indptr + b + 1) - __ldg(a.qo_indptr + b) != 0)
-        flag_error(a.dev_err, PNKV_DEV_ERR_QO_INDPTR);
+      const int e = seq_errors(a, q0, qlen, len);
+      if (e) flag_error(a.dev_err, e);
       for (int h = 0; h < a.hkv; ++h) {
         a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h)] = 0;
         a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h) + 1] = 0;
@@ -782,21 +1014,28 @@ int prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t m
   return 1;
 }
 
-// Launch the tensor-core tile path (called by paged_decode_attention when a KV
-// head has more than 64 query rows).
+// Launch the tensor-core tile path: called by paged_decode_attention when a KV
+// head has more than 64 query rows (q_scale = 0: fp16 queries), and by
+// paged_prefill_attention_fp4q (q_scale = g_Q > 0: NVFP4 queries, block-scaled
+// FP4 QK^T).
 int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32_t* qo_indptr,
                    const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
-                   int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal, float* o_part,
-                   float* lse_part, int64_t part_slots, int32_t* work_meta, int32_t* dev_err,
-                   cudaStream_t stream) {
+                   int64_t total_q, int32_t num_q_heads, int32_t max_qlen, float sm_scale, int32_t causal,
+                   float q_scale, float* o_part, float* lse_part, int64_t part_slots, int32_t* work_meta,
+                   int32_t* dev_err, cudaStream_t stream) {
   if (cache->dtype != PNKV_KV_NVFP4) return PNKV_ERR_UNSUPPORTED;
+  const bool fp4q = q_scale > 0.f;
   PrefillArgs a;
   a.num_pages = cache->num_pages;
   a.hkv = cache->num_kv_heads;
   a.group = num_q_heads / cache->num_kv_heads;
   a.tpt = 128 / a.group;
-  a.qk_scale_log2 = sm_scale * cache->k_scale * kLog2e;
+  // logit = (q . k) * sm_scale; the products run on codes times block scales,
+  // so the per-tensor decode scales of K (and of Q for FP4 queries) multiply here
+  a.qk_scale_log2 = sm_scale * cache->k_scale * (fp4q ? q_scale : 1.f) * kLog2e;
   a.out_scale = cache->v_scale;
+  a.q_scale = fp4q ? q_scale : 0.f;
+  a.q_enc = fp4q ? static_cast<float>(1.0 / (6.0 * static_cast<double>(q_scale))) : 0.f;
   a.q = q_roped;
   a.qo_indptr = qo_indptr;
   a.page_table = page_table;
@@ -807,28 +1046,37 @@ int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32
   a.max_qlen = max_qlen;
   a.rows_per_slot = a.group * max_qlen;
   a.causal = causal ? 1 : 0;
+  a.total_q = total_q;
+  a.wait_ns = pipeline_wait_ns();
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.part_slots = part_slots;
   a.work_meta = work_meta;
   a.dev_err = dev_err;
-  CUtensorMap map;
-  int st = make_pool_map(cache, 36, &map);
+  // the pool as 128-byte rows, 36 per head record: whole-record boxes for the
+  // fp16 tile; for the FP4 tile a box of the 20 rows after the K codes and a
+  // box of the 16 K-code rows
+  CUtensorMap map, map_k;
+  int st = make_pool_map_box(cache, 36, fp4q ? Plan<true>::kRawRows : Plan<false>::kRawRows, &map);
   if (st != PNKV_OK) return st;
+  if (fp4q) {
+    if ((st = make_pool_map_box(cache, 36, 16, &map_k)) != PNKV_OK) return st;
+  } else {
+    map_k = map;
+  }
   int sms = 0;
   if ((st = device_sm_count(&sms)) != PNKV_OK) return st;
   a.splits = prefill_splits(batch, a.hkv, a.group, max_qlen, sms);
   if (part_slots < static_cast<int64_t>(batch) * a.hkv * a.splits) return PNKV_ERR_INVALID_ARG;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(prefill_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return PNKV_ERR_CUDA;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured_f16{0}, configured_fp4{0};  // devices whose attribute is set
+  const void* kern = fp4q ? reinterpret_cast<const void*>(prefill_tile_kernel<true>)
+                          : reinterpret_cast<const void*>(prefill_tile_kernel<false>);
+  const int smem = fp4q ? Layout<true>::kSmemBytes : Layout<false>::kSmemBytes;
+  if ((st = set_smem_limit_once(fp4q ? configured_fp4 : configured_f16, kern, smem)) != PNKV_OK) return st;
   st = launch_pdl(prefill_meta_kernel, dim3((batch + 255) / 256), dim3(256), 0, stream, a);
   if (st != PNKV_OK) return st;
-  return launch_pdl(prefill_tile_kernel, dim3(sms), dim3(kThreads), kSmemBytes, stream, map, a);
+  if (fp4q) return launch_pdl(prefill_tile_kernel<true>, dim3(sms), dim3(kThreads), smem, stream, map, map_k, a);
+  return launch_pdl(prefill_tile_kernel<false>, dim3(sms), dim3(kThreads), smem, stream, map, map_k, a);
 }
 
 }  // namespace pnkv

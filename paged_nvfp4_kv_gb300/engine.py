@@ -14,8 +14,9 @@ import math
 import numpy as np
 import torch
 
-from . import (Cache, decode_slots, kv_append_nvfp4, paged_decode_attention, split_kv_combine,
-               work_meta_ints, yarn_params, yarn_rope_tables)
+from . import (Cache, decode_slots, kv_append_nvfp4, paged_decode_attention,
+               paged_prefill_attention_fp4q, split_kv_combine, work_meta_ints, yarn_params,
+               yarn_rope_tables)
 
 
 def to_bf16(x, device):
@@ -98,48 +99,83 @@ class DecodeSession:
                         self.q, self.q_roped, self.k, self.v, self.cos, self.sin, self.rotary_dim,
                         self.dev_err, self.stream)
 
-    def attend(self, out_fp32=False):
+    def attend(self, out_fp32=False, q_scale=None):
+        """Attention of the step's roped queries -> combined output.  With
+        ``q_scale`` (a prefill chunk on an NVFP4 pool) the queries are NVFP4-
+        encoded with that decode scale and QK^T runs block-scaled in FP4."""
+        self.partials(q_scale)
+        return self.combine(out_fp32)
+
+    def partials(self, q_scale=None):
+        """The attention call alone: per-split partials into o_part/lse_part."""
         w = self.w
-        paged_decode_attention(self.cache, self.q_roped, self.qo_indptr, self.page_table,
-                               self.seq_lens, w.num_q_heads, self.max_qlen, self.sm_scale,
-                               w.causal, self.o_part, self.lse_part, self.work_meta, self.dev_err,
-                               self.stream)
+        if q_scale is None:
+            paged_decode_attention(self.cache, self.q_roped, self.qo_indptr, self.page_table,
+                                   self.seq_lens, w.num_q_heads, self.max_qlen, self.sm_scale,
+                                   w.causal, self.o_part, self.lse_part, self.work_meta,
+                                   self.dev_err, self.stream)
+        else:
+            paged_prefill_attention_fp4q(self.cache, self.q_roped, self.qo_indptr, self.page_table,
+                                         self.seq_lens, w.num_q_heads, self.max_qlen, self.sm_scale,
+                                         w.causal, q_scale, self.o_part, self.lse_part,
+                                         self.work_meta, self.dev_err, self.stream)
+
+    def combine(self, out_fp32=False):
+        """The log-sum-exp merge of the partials -> out (bf16) or out32."""
+        w = self.w
         out = self.out32 if out_fp32 else self.out
         split_kv_combine(self.o_part, self.lse_part, self.work_meta, self.qo_indptr, self.total_q,
                          w.num_q_heads, w.num_kv_heads, self.max_qlen, out, self.lse, self.stream)
         return out
 
-    def step(self, out_fp32=False):
+    def step(self, out_fp32=False, q_scale=None):
         self.append()
-        return self.attend(out_fp32)
+        return self.attend(out_fp32, q_scale)
 
     def error_word(self):
         return int(self.dev_err.item())
 
 
 class DecodeStack:
-    """``layers`` attention layers of one geometry, each with its own pool,
-    stepped together; the step can be captured in a CUDA graph and replayed
-    (the library allocates nothing and every call is stream-ordered, so a
-    captured step is the same launches with the same arguments).
+    """Attention layers of one geometry, each with its own pool, stepped
+    together; the step can be captured in a CUDA graph and replayed (the
+    library allocates nothing and every call is stream-ordered, so a captured
+    step is the same launches with the same arguments).
 
-    Layer 0 is filled from the workload; the other layers start as copies of
-    its pool (identical caches, distinct memory), and all layers append the
-    same new tokens."""
+    ``workloads`` holds one workload per layer: each layer has its own seeded
+    K/V, new tokens, page table and per-tensor scales, and is filled from its
+    own workload.  ``replicated(w, layers)`` builds a stack whose layers
+    start as byte copies of layer 0's pool and append layer 0's new tokens
+    (distinct memory, identical contents): the same work per layer, for timing
+    deep stacks without drawing every layer's cache on the host."""
 
-    def __init__(self, w, layers=16, device="cuda"):
-        first = DecodeSession(w, device=device)
+    def __init__(self, workloads, device="cuda", _replicas=0):
+        first = DecodeSession(workloads[0], device=device,
+                              max_pos=max(w.max_pos for w in workloads))
         self.sessions = [first]
-        for _ in range(layers - 1):
-            self.sessions.append(DecodeSession(w, device=device, tables=(first.cos, first.sin),
-                                               inputs=first))
+        self.replicated_from_first = _replicas > 0
+        for _ in range(_replicas):
+            self.sessions.append(DecodeSession(workloads[0], device=device, max_pos=first.max_pos,
+                                               tables=(first.cos, first.sin), inputs=first))
+        for w in workloads[1:]:
+            if w.yarn != workloads[0].yarn:
+                raise ValueError("the layers of a stack share one rope table: YaRN parameters differ")
+            self.sessions.append(DecodeSession(w, device=device, max_pos=first.max_pos,
+                                               tables=(first.cos, first.sin)))
         self.graph = None
+
+    @classmethod
+    def replicated(cls, w, layers=16, device="cuda"):
+        return cls([w], device=device, _replicas=layers - 1)
 
     def fill(self):
         first = self.sessions[0]
         first.fill()
         for s in self.sessions[1:]:
-            s.cache.pool.copy_(first.cache.pool)
+            if self.replicated_from_first:
+                s.cache.pool.copy_(first.cache.pool)
+            else:
+                s.fill()
 
     def step(self, out_fp32=False):
         return [s.step(out_fp32) for s in self.sessions]

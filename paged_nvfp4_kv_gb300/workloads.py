@@ -102,6 +102,13 @@ class Workload:
         return float(np.float32(6.0 * float(self.c_k.max()) * m * math.sqrt(2.0) / self._code_top))
 
     @property
+    def g_q(self):
+        """Per-tensor decode scale for NVFP4-encoded queries (the FP4-query
+        prefill): as g_k, from the widest query channel (E2M1 x E4M3 range)."""
+        m = 0.1 * math.log(self.yarn["factor"]) + 1.0 if self.yarn["factor"] > 1 else 1.0
+        return float(np.float32(6.0 * float(self.c_q.max()) * m * math.sqrt(2.0) / (E2M1_TOP * E4M3_TOP)))
+
+    @property
     def g_v(self):
         return float(np.float32(6.0 * float(self.c_v.max()) / self._code_top))
 
@@ -211,6 +218,16 @@ def multi_session_verify(seed=1004, sessions=16):
                  [5] * sessions)
 
 
+def multi_session_verify_reduced(seed=1004, sessions=16):
+    """The multi-session verify shape at a quarter of its lengths (log-uniform
+    in [2,048, 131,072], about 0.5M keys, pool larger than L2), for kernel
+    profiles that must stay small (profiling only)."""
+    rng = np.random.default_rng([seed, _TENSOR_ID["lens"]])
+    lens = np.floor(_log_uniform(rng, 2048, 131072, sessions)).astype(np.int64)
+    return build("multi-session verify, reduced (16 x qlen 5, NVFP4)", seed, "nvfp4", lens,
+                 [5] * sessions)
+
+
 def chunked_prefill(seed=1005):
     """1 sequence with 1,040,384 cached NVFP4 tokens plus an 8,192-token chunk."""
     return build("chunked prefill (8,192 queries over 1,048,576 NVFP4 keys)", seed, "nvfp4",
@@ -236,4 +253,5 @@ def million_token_decode_int8(seed=1003):
 
 WORKLOADS = {1: tiny_decode, 2: native_window_decode, 3: million_token_decode,
            4: multi_session_verify, 5: chunked_prefill, 6: chunked_prefill_reduced,
-           7: million_token_decode_fp8, 8: million_token_decode_int8}
+           7: million_token_decode_fp8, 8: million_token_decode_int8,
+           9: multi_session_verify_reduced}

@@ -34,8 +34,18 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_text(lib):
-    assert lib.pnkv_version() == 100
+    assert lib.pnkv_version() == 200
     assert lib.pnkv_status_string(-1) == b"invalid argument"
+
+
+def test_wait_limit_setting(lib):
+    """The pipeline wait bound is a host setting; out-of-range values are
+    rejected and the previous bound is returned (no GPU involved)."""
+    assert lib.pnkv_set_wait_limit_ns(999) == _lib.PNKV_ERR_INVALID_ARG
+    assert lib.pnkv_set_wait_limit_ns(61 * 10**9) == _lib.PNKV_ERR_INVALID_ARG
+    prev = lib.pnkv_set_wait_limit_ns(5000)
+    assert prev == 2 * 10**9
+    assert lib.pnkv_set_wait_limit_ns(prev) == 5000
 
 
 def _yarn(**kw):
@@ -114,16 +124,19 @@ def test_append_validation(lib):
 def test_decode_and_combine_validation(lib):
     c = _cache()
     P = ctypes.c_void_p
-    args = [ctypes.byref(c), P(256), P(256), P(256), 4, P(256), 1, 24, 1, 0.0625, 1, P(256),
+    args = [ctypes.byref(c), P(256), P(256), P(256), 4, P(256), 1, 1, 24, 1, 0.0625, 1, P(256),
             P(256), 1000, P(256), P(256), None]
     bad = list(args)
-    bad[9] = float("nan")
+    bad[10] = float("nan")
     assert lib.paged_decode_attention(*bad) == -1
     bad = list(args)
-    bad[7] = 25                      # not a multiple of the KV heads
+    bad[8] = 25                      # not a multiple of the KV heads
     assert lib.paged_decode_attention(*bad) == -1
     bad = list(args)
     bad[1] = None
+    assert lib.paged_decode_attention(*bad) == -1
+    bad = list(args)
+    bad[7] = -1                      # total_q
     assert lib.paged_decode_attention(*bad) == -1
     assert lib.pnkv_work_meta_ints(16, 4) == 4 + 2 * 64
     assert lib.pnkv_work_meta_ints(0, 4) == -1

@@ -50,10 +50,9 @@ def _check(w, s, out32, out16, rows, sample_pages):
     pool = s.cache.pool.cpu().numpy().reshape(w.num_pages, -1)
     for b, positions in sample_pages.items():
         for page, (want, used) in oracle_path.pool_pages(w, cos_t, sin_t, b, positions).items():
-            if used == 16:
-                assert np.array_equal(pool[page], want), (b, page)
-            else:  # a partly filled last page: compare the written slots' bytes
-                assert np.array_equal(pool[page][want != 0], want[want != 0]), (b, page)
+            # every byte of the page, zeros included: a partly filled last page's
+            # unwritten slots stay as the zero-filled pool left them
+            assert np.array_equal(pool[page], want), (b, page, used)
     ref = oracle_path.attention(w, pool, q, rows=set(rows))
     o = out32.cpu().numpy()
     errs = np.concatenate([np.abs(o[t, h] - ref[(t, h)][0]) for (t, h) in rows])
@@ -137,3 +136,34 @@ def test_chunked_prefill_full():
     rows = sorted(set(zip(toks.tolist(), heads.tolist())))
     _check(w, s, o32, o16, rows, {0: [0, 1040383, 1040384, 1044000, 1048575]
                                        + list(rng.integers(0, 1048576, 8))})
+
+
+def test_chunked_prefill_fp4q_full():
+    """The FP4-query tile (block-scaled FP4 QK^T): 256 seeded rows of the
+    8,192-token chunk over up to 1,048,576 keys against the oracle's
+    attention with the queries' NVFP4 round trip."""
+    from oracle import fp4_prefill as FP
+    from paged_nvfp4_kv_gb300 import workloads as W
+    from paged_nvfp4_kv_gb300.engine import DecodeSession
+    w = W.chunked_prefill()
+    s = DecodeSession(w)
+    s.fill()
+    s.append()
+    out32 = s.attend(out_fp32=True, q_scale=w.g_q).clone()
+    out16 = s.attend(out_fp32=False, q_scale=w.g_q).clone()
+    torch.cuda.synchronize()
+    assert s.error_word() == 0
+    rng = np.random.default_rng(1005)
+    toks = rng.integers(0, 8192, 256)
+    heads = rng.integers(0, 24, 256)
+    rows = sorted(set(zip(toks.tolist(), heads.tolist())))
+    q = s.q_roped.float().cpu().numpy().astype(np.float64)
+    q_hat = FP.dequantized_queries(q, w.g_q)
+    pool = s.cache.pool.cpu().numpy().reshape(w.num_pages, -1)
+    ref = oracle_path.attention(w, pool, q_hat, rows=set(rows))
+    o = out32.cpu().numpy()
+    errs = np.concatenate([np.abs(o[t, h] - ref[(t, h)][0]) for (t, h) in rows])
+    assert errs.max() <= MAX_ABS, errs.max()
+    assert errs.mean() <= MEAN_ABS, errs.mean()
+    want16 = torch.from_numpy(o).to(torch.bfloat16)
+    assert torch.equal(out16.cpu().view(torch.int16), want16.view(torch.int16))

@@ -35,6 +35,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "decode_common.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -46,6 +47,7 @@ int launch_prefill(const pnkv_cache* cache, const uint16_t* q_roped, const int32
                    float q_scale, float* o_part, float* lse_part, int64_t part_slots, int32_t* work_meta,
                    int32_t* dev_err, cudaStream_t stream);
 int prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t max_qlen, int sms);
+int launch_verify(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream);
 
 namespace {
 
@@ -66,30 +68,6 @@ struct Consumers {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct DecodeArgs {
-  int64_t num_pages;
-  int32_t hkv;
-  int32_t group;          // query heads per KV head
-  float qk_scale_log2;    // sm_scale * log2(e) (* k_scale for NVFP4 and FP8)
-  float out_scale;        // v_scale for NVFP4 and FP8, 1 for INT8 and bf16
-  const uint16_t* q;      // roped bf16 queries [total_q, hq, 256]
-  const int32_t* qo_indptr;
-  const int32_t* page_table;
-  int64_t pt_stride;
-  const int32_t* seq_lens;
-  int32_t batch;
-  int64_t total_q;        // rows of q (qo_indptr[batch] must not exceed it)
-  int32_t hq;
-  int32_t max_qlen;
-  int32_t rows_per_slot;  // group * max_qlen
-  int32_t causal;
-  uint64_t wait_ns;       // bound of a pipeline wait
-  float* o_part;
-  float* lse_part;
-  int64_t part_slots;
-  int32_t* work_meta;
-  int32_t* dev_err;
-};
 
 template <int KVDT>
 struct Geometry;
@@ -116,134 +94,6 @@ struct Geometry<PNKV_KV_BF16> {
   static constexpr int kBoxRows = 128;     // 16,384 B head record
   static constexpr int kStageBytes = 16384;
   static constexpr uint32_t kTxBytes = 16384;
-};
-
-// ---------------------------------------------------------------------------
-// Sequence walk: unit counts per sequence and the segment containing a unit.
-// Every thread of a CTA runs the same walk, so all agree on the pieces.
-
-struct SeqInfo {
-  int32_t len;    // keys
-  int32_t qlen;   // new query rows (tokens)
-  int32_t q0;     // qo_indptr[b]
-  int32_t pages;  // units per (b, h); 0 if the sequence has no valid work
-};
-
-__device__ __forceinline__ SeqInfo load_seq(const DecodeArgs& a, int b, bool flag) {
-  SeqInfo s;
-  s.len = __ldg(a.seq_lens + b);
-  s.q0 = __ldg(a.qo_indptr + b);
-  s.qlen = __ldg(a.qo_indptr + b + 1) - s.q0;
-  s.pages = (s.len + 15) >> 4;
-  bool ok = true;
-  if (s.qlen < 0 || s.qlen > a.max_qlen || s.qlen > s.len || s.q0 < 0 ||
-      static_cast<int64_t>(s.q0) + s.qlen > a.total_q) {
-    if (flag) flag_error(a.dev_err, PNKV_DEV_ERR_QO_INDPTR);
-    ok = false;
-  }
-  if (s.len < 0 || static_cast<int64_t>(s.pages) > a.pt_stride) {
-    if (flag) flag_error(a.dev_err, PNKV_DEV_ERR_SEQ_LEN);
-    ok = false;
-  }
-  if (!ok || s.qlen == 0) s.pages = 0;
-  return s;
-}
-
-// Total units over all sequences (warp-cooperative; every lane gets it).
-__device__ __forceinline__ int64_t total_units(const DecodeArgs& a, int lane) {
-  int64_t tot = 0;
-  for (int b0 = 0; b0 < a.batch; b0 += 32) {
-    const int b = b0 + lane;
-    int64_t u = 0;
-    if (b < a.batch) u = static_cast<int64_t>(load_seq(a, b, true).pages) * a.hkv;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-    tot += u;
-  }
-  return tot;
-}
-
-// Find the sequence b whose unit range [base, base + hkv * pages) contains
-// `u` (warp-cooperative).  Returns b and its base.
-__device__ __forceinline__ void find_seq(const DecodeArgs& a, int64_t u, int lane, int* b_out,
-                                         int64_t* base_out) {
-  int64_t base = 0;
-  for (int b0 = 0; b0 < a.batch; b0 += 32) {
-    const int b = b0 + lane;
-    int64_t cnt = 0;
-    if (b < a.batch) cnt = static_cast<int64_t>(load_seq(a, b, false).pages) * a.hkv;
-    // inclusive scan
-    int64_t inc = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += t;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, b < a.batch && base + inc > u);
-    if (hit) {
-      const int first = __ffs(hit) - 1;
-      const int64_t excl = __shfl_sync(0xffffffffu, inc - cnt, first);
-      *b_out = b0 + first;
-      *base_out = base + excl;
-      return;
-    }
-    base += __shfl_sync(0xffffffffu, inc, 31);
-  }
-  *b_out = a.batch;
-  *base_out = base;
-}
-
-// A maximal run of this CTA's units inside one (b, h) segment.
-struct Piece {
-  int b, h;
-  SeqInfo s;
-  int64_t seg_start;  // flattened unit index of the segment's first unit
-  int32_t p0;         // first page (index within the sequence)
-  int32_t n;          // units in this piece
-  int64_t i0;         // CTA-local index of the piece's first unit
-};
-
-struct Walker {
-  int b, h;
-  SeqInfo s;
-  int64_t seg_start;
-  int64_t u, u_end, u_begin;
-  bool valid;
-
-  __device__ void init(const DecodeArgs& a, int64_t begin, int64_t end, int lane) {
-    u_begin = u = begin;
-    u_end = end;
-    valid = begin < end;
-    if (!valid) return;
-    int64_t base;
-    find_seq(a, begin, lane, &b, &base);
-    s = load_seq(a, b, false);
-    h = static_cast<int>((begin - base) / s.pages);
-    seg_start = base + static_cast<int64_t>(h) * s.pages;
-  }
-
-  // Next piece; false when the CTA's range is done.
-  __device__ bool next(const DecodeArgs& a, Piece* pc) {
-    if (!valid || u >= u_end) return false;
-    while (u >= seg_start + s.pages) {  // advance to the segment holding u
-      seg_start += s.pages;
-      if (++h == a.hkv) {
-        h = 0;
-        ++b;
-        s = load_seq(a, b, false);
-      }
-    }
-    pc->b = b;
-    pc->h = h;
-    pc->s = s;
-    pc->seg_start = seg_start;
-    pc->p0 = static_cast<int32_t>(u - seg_start);
-    const int64_t stop = min(u_end, seg_start + s.pages);
-    pc->n = static_cast<int32_t>(stop - u);
-    pc->i0 = u - u_begin;
-    u = stop;
-    return true;
-  }
 };
 
 // ---------------------------------------------------------------------------
@@ -885,7 +735,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   griddep_launch_dependents();
 
   // this CTA's unit range
-  const int64_t total = total_units(a, lane);
+  const int64_t total = total_units<1>(a, lane);
   const int64_t chunk = (total + gridDim.x - 1) / gridDim.x;
   const int64_t u_begin = min(total, static_cast<int64_t>(blockIdx.x) * chunk);
   const int64_t u_end = min(total, u_begin + chunk);
@@ -900,14 +750,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // segments without units get an empty slot range here; every other
     // segment's range is written by the CTA that holds its first unit
     for (int b = lane; b < a.batch; b += 32)
-      if (load_seq(a, b, false).pages == 0)
+      if (load_seq<1>(a, b, false).units == 0)
         for (int h = 0; h < a.hkv; ++h) {
           a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h)] = 0;
           a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h) + 1] = 0;
         }
   }
 
-  Walker walk;
+  Walker<1> walk;
   walk.init(a, u_begin, u_end, lane);
   Piece pc;
 
@@ -915,12 +765,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // are, before any work (so the record exists even if the call winds down
   // after a timeout)
   if (threadIdx.x == 0) {
-    Walker w0 = walk;
+    Walker<1> w0 = walk;
     while (w0.next(a, &pc)) {
       if (pc.p0 != 0) continue;
       const int64_t seg = pc.b * static_cast<int64_t>(a.hkv) + pc.h;
       const int64_t first_cta = pc.seg_start / chunk;
-      const int64_t last_cta = (pc.seg_start + pc.s.pages - 1) / chunk;
+      const int64_t last_cta = (pc.seg_start + pc.s.units - 1) / chunk;
       a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg + first_cta);
       a.work_meta[4 + 2 * seg + 1] = static_cast<int32_t>(last_cta - first_cta + 1);
     }
@@ -1246,6 +1096,9 @@ int dispatch_rows(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStr
   if (rows <= 8)
     return launch_decode<KVDT, 1, 1, fp4 ? PNKV_NVFP4_NW : 7, fp4 ? PNKV_NVFP4_QS : 0, fp4 ? PNKV_NVFP4_NP : 1>(
         map, a, grid, stream);
+  // 9 .. 32 rows on an NVFP4 pool (speculative verify): the tensor-core tile
+  // with the keys as the M dimension, K and V widened once per page-head
+  if (KVDT == PNKV_KV_NVFP4 && rows <= 32) return launch_verify(map, a, grid, stream);
   if (rows <= 16) return launch_decode<KVDT, 2, 1, 7, PNKV_WIDE_QS, PNKV_WIDE_NP>(map, a, grid, stream);
   if (rows <= 32) return launch_decode<KVDT, 2, 2, 7, PNKV_WIDE_QS, PNKV_WIDE_NP>(map, a, grid, stream);
   if (rows <= 64) return launch_decode<KVDT, 2, 4, 5, PNKV_WIDE_QS, PNKV_WIDE_NP>(map, a, grid, stream);

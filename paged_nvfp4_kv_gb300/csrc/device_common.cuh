@@ -68,14 +68,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same with a bound on how long the thread may be suspended inside the test.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
-// (and the caller flags a timeout) if that takes longer than limit_ns.
+// (and the caller flags a timeout) if that takes longer than limit_ns.  Each
+// test may suspend the thread for at most a quarter of the bound (at most
+// 100 us), and the clock is read after every test, so a short bound is kept
+// to within about a quarter of itself.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = static_cast<uint32_t>(limit_ns / 4 < 100000ull ? limit_ns / 4 : 100000ull);
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  for (;;) {
+    if (mbar_try_wait_for(bar, parity, hint)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

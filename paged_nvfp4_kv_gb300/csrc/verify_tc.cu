@@ -1,0 +1,695 @@
+// Split-KV GQA attention on the 5th-generation tensor cores for KV heads with
+// 9 .. 32 query rows per step: speculative-decoding verify, a few new tokens
+// per sequence times the GQA group ("Ten Cards, Over 100 tok/s": four draft
+// tokens need five query columns per session), over a paged NVFP4 cache
+// ("262,144 Tokens on One RTX 5090", section "Why NVFP4 KV changes the
+// math").
+//
+// The attention and its numerics are those of the register-tile decode path
+// (q k^T * sm_scale with K, V widened exactly to fp16 from E2M1 x E4M3, fp32
+// logits, fp16 probabilities in P.V, fp32 accumulation).  What changes is the
+// orientation.  With 30 rows per KV head a row-major tensor-core tile would
+// be mostly padding, and mma.sync would need 128 m16n8k16 per page and head,
+// more tensor time than the page's bytes take to arrive.  Here the keys are
+// the M dimension: a unit is 128 keys (8 pages) of one (sequence, KV head),
+//   S^T [128 keys x 32 rows]  = K [128 x 256] . Q^T      (16 MMAs, M128 N32 K16)
+//   O^T [256 dims x 32 rows] += V^T [256 x 128] . P^T    (2 x 8 MMAs)
+// with K and V^T widened once per unit straight into TMEM as the A operands
+// (lane = key for K, lane = dim for V^T; two fp16 per column), Q^T and P^T
+// as the B operands in shared memory, S^T and O^T accumulating in TMEM.
+// Each page-head's codes are read from HBM once and widened once, whatever
+// the number of query rows.
+//
+// Roles (15 warps):
+//   softmax warps 0-3   one key per thread (TMEM lane), 32 rows per thread:
+//                       tcgen05.ld of S^T, mask, exponentials against a per-
+//                       row reference maximum that moves only when a row's
+//                       logits pass it by more than 2^8 (then the exact block
+//                       maxima are reduced and O^T and the row sums rescaled),
+//                       P^T (fp16) to shared memory, per-thread row sums
+//   K warps 4-7         K codes x block scales -> fp16 K rows in TMEM
+//   V warps 8-11        V codes x block scales -> fp16 V^T rows in TMEM (the
+//                       pool stores V slot-pair interleaved, so one code byte
+//                       widens to the key pair one TMEM column holds)
+//   producer warp 12    one 2-D TMA load per page (the head record) into a
+//                       4-stage ring
+//   warp 13             allocates TMEM, issues the QK products
+//   warp 14             issues the P.V products
+// Work is split stream-K over (sequence, KV head, unit) exactly as the decode
+// path splits its pages, with the same partial slots, so split_kv_combine
+// merges the pieces.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+
+#include <cudaTypedefs.h>
+
+#include "decode_common.cuh"
+#include "device_common.cuh"
+#include "host_common.h"
+#include "tcgen05.cuh"
+
+namespace pnkv {
+namespace {
+
+constexpr int kThreadsV = 480;
+constexpr int kKWarp0 = 4, kVWarp0 = 8, kProdWarp = 12, kQkWarp = 13, kPvWarp = 14;
+constexpr int kUnitPages = 8;
+constexpr int kUnitKeys = 16 * kUnitPages;  // 128: the M of the products
+constexpr int kRowsN = 32;                  // query rows per KV head covered (N)
+constexpr int kRawStages = 4;
+constexpr int kRawPage = 5120;              // 4,608-byte record in a 1,024-aligned slot
+constexpr int kRawStage = kUnitPages * kRawPage;
+constexpr uint32_t kRecBytesV = 4608;
+constexpr int kPStages = 2;
+constexpr float kLn2V = 0.6931471805599453f;
+constexpr float kMoveThreshold = 8.f;       // log2 units
+
+// shared memory (from a 1,024-aligned base)
+constexpr int kRawOff = 0;
+constexpr int kQOff = kRawOff + kRawStages * kRawStage;  // Q^T: fp16 [32 rows][256 dims], core matrices
+constexpr int kQBytes = kRowsN * 256 * 2;
+// P^T: fp16 [32 rows][128 keys], 8x8 core matrices with padded strides:
+// 144 bytes between neighbours along the keys and 2,336 between 8-row
+// groups, so that the 32 stores of a warp (16 key pairs, two row groups)
+// fall on distinct banks
+constexpr int kPLbo = 144, kPSbo = 16 * kPLbo + 32;
+constexpr int kPOff = kQOff + kQBytes;
+constexpr int kPBytes = 4 * kPSbo;
+constexpr int kScrOff = kPOff + kPStages * kPBytes;      // per V warp: scales [page][4 blocks][16 slots]
+constexpr int kScrWarp = kUnitPages * 4 * 16;
+constexpr int kMrefOff = kScrOff + 4 * kScrWarp;         // float [32]: per-row reference maximum (log2)
+constexpr int kLimOff = kMrefOff + kRowsN * 4;           // int [32]: keys row r may see
+constexpr int kAlphaOff = kLimOff + kRowsN * 4;          // float [32]: rescale factors
+constexpr int kXchgOff = kAlphaOff + kRowsN * 4;         // float [4 warps][32]: reductions
+constexpr int kFlagOff = kXchgOff + 4 * kRowsN * 4;      // uint [4]: softmax warps' flags
+constexpr int kBarOffV = (kFlagOff + 16 + 7) & ~7;
+enum {
+  V_RAW_FULL = 0,
+  V_RAW_EMPTY = V_RAW_FULL + kRawStages,
+  V_K_FULL = V_RAW_EMPTY + kRawStages,
+  V_K_FREE = V_K_FULL + 2,
+  V_V_FULL = V_K_FREE + 2,
+  V_V_FREE = V_V_FULL + 1,
+  V_S_FULL = V_V_FREE + 1,
+  V_S_FREE = V_S_FULL + 2,
+  V_P_FULL = V_S_FREE + 2,
+  V_PV_DONE = V_P_FULL + kPStages,
+  V_Q_FULL = V_PV_DONE + kPStages,
+  V_FINAL = V_Q_FULL + 1,
+  kNumBarsV = V_FINAL + 1
+};
+constexpr int kMiscOffV = kBarOffV + kNumBarsV * 8;  // tmem base, abort flag, raw valid[4], armed[4]
+constexpr int kSmemV = kMiscOffV + 64 + 1024;
+static_assert(kSmemV <= 232448, "verify tile shared memory plan too large");
+static_assert(kQOff % 1024 == 0, "raw ring slots need 1,024-byte alignment");
+
+// TMEM columns: K (two stages of 128), V^T (halves of 64), S^T (two stages
+// of 32), O^T (halves of 32)
+constexpr uint32_t kTmemColsV = 512;
+constexpr uint32_t kTK = 0, kTV = 256, kTS = 384, kTO = 448;
+
+__device__ __forceinline__ uint64_t* vbar(uint8_t* smem, int i) {
+  return reinterpret_cast<uint64_t*>(smem + kBarOffV) + i;
+}
+
+__device__ __forceinline__ uint32_t par(int64_t g, int n) { return static_cast<uint32_t>((g / n) & 1); }
+
+// Byte offset of P^T element (row r, key k).
+__device__ __forceinline__ uint32_t p_off(int r, int k) {
+  return (r >> 3) * kPSbo + (k >> 3) * kPLbo + ((r & 7) << 4) + ((k & 7) << 1);
+}
+
+// The 32-bit TMEM word of a warp's lane quarter: lane 32 * quarter, column c.
+__device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int quarter) {
+  return tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+}
+
+__global__ void __launch_bounds__(kThreadsV, 1)
+    verify_tile_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMiscOffV);
+  volatile uint32_t* abort_flag = misc + 1;
+  uint32_t* raw_valid = misc + 2;            // [kRawStages] bit j: page j of the unit loaded
+  int32_t* raw_armed = reinterpret_cast<int32_t*>(misc + 6);  // [kRawStages] unit that armed the stage
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return vbar(smem, i); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(bar(V_RAW_FULL + i), 1);
+      mbar_init(bar(V_RAW_EMPTY + i), 8);  // the K and the V warps
+      raw_armed[i] = -1;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(V_K_FULL + i), 4);
+      mbar_init(bar(V_K_FREE + i), 1);
+      mbar_init(bar(V_S_FULL + i), 1);
+      mbar_init(bar(V_S_FREE + i), 4);
+    }
+    mbar_init(bar(V_V_FULL), 4);
+    mbar_init(bar(V_V_FREE), 1);
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(bar(V_P_FULL + i), 4);
+      mbar_init(bar(V_PV_DONE + i), 1);
+    }
+    mbar_init(bar(V_Q_FULL), 4);
+    mbar_init(bar(V_FINAL), 2);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kQkWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(misc)),
+                 "r"(kTmemColsV)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  if (warp == kProdWarp && lane == 0) tma_prefetch_desc(&tmap);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // this CTA's unit range, as in the decode path
+  const int64_t total = total_units<kUnitPages>(a, lane);
+  const int64_t chunk = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t u_begin = min(total, static_cast<int64_t>(blockIdx.x) * chunk);
+  const int64_t u_end = min(total, u_begin + chunk);
+  if (blockIdx.x == 0 && warp == 0) {
+    if (lane == 0) {
+      a.work_meta[0] = a.hkv;
+      a.work_meta[1] = a.group;
+      a.work_meta[2] = a.rows_per_slot;
+      a.work_meta[3] = a.batch;
+    }
+    for (int b = lane; b < a.batch; b += 32)
+      if (load_seq<kUnitPages>(a, b, false).units == 0)
+        for (int h = 0; h < a.hkv; ++h) {
+          a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h)] = 0;
+          a.work_meta[4 + 2 * (static_cast<int64_t>(b) * a.hkv + h) + 1] = 0;
+        }
+  }
+  Walker<kUnitPages> walk;
+  walk.init(a, u_begin, u_end, lane);
+  Piece pc;
+  if (threadIdx.x == 0) {  // slot ranges of the segments that start here, before any work
+    Walker<kUnitPages> w0 = walk;
+    while (w0.next(a, &pc)) {
+      if (pc.p0 != 0) continue;
+      const int64_t seg = pc.b * static_cast<int64_t>(a.hkv) + pc.h;
+      const int64_t first_cta = pc.seg_start / chunk;
+      const int64_t last_cta = (pc.seg_start + pc.s.units - 1) / chunk;
+      a.work_meta[4 + 2 * seg] = static_cast<int32_t>(seg + first_cta);
+      a.work_meta[4 + 2 * seg + 1] = static_cast<int32_t>(last_cta - first_cta + 1);
+    }
+  }
+
+  auto fail = [&]() {
+    flag_error(a.dev_err, PNKV_DEV_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+  auto wait1 = [&](int b, uint32_t parity) -> bool {  // one thread
+    if (mbar_try_wait(bar(b), parity)) return true;
+    if (*abort_flag) return false;
+    if (!mbar_wait(bar(b), parity, a.wait_ns)) {
+      fail();
+      return false;
+    }
+    return true;
+  };
+  auto waitw = [&](int b, uint32_t parity) -> bool {  // warp-uniform
+    bool ok = !*abort_flag && mbar_wait(bar(b), parity, a.wait_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) fail();
+    return ok;
+  };
+
+  if (warp == kProdWarp) {
+    // ---------------------------------------------------------- producer
+    const uint64_t policy = l2_policy_evict_first();
+    int64_t g = 0;
+    bool ok = true;
+    while (ok && walk.next(a, &pc)) {
+      const int32_t* row = a.page_table + static_cast<int64_t>(pc.b) * a.pt_stride;
+      for (int k = 0; k < pc.n && ok; ++k, ++g) {
+        const int rs = static_cast<int>(g % kRawStages);
+        if (lane == 0) ok = wait1(V_RAW_EMPTY + rs, par(g, kRawStages) ^ 1u);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        int32_t page = -1;
+        if (lane < kUnitPages) {
+          const int pi = (pc.p0 + k) * kUnitPages + lane;
+          if (pi < pc.s.pages) {
+            page = __ldg(row + pi);
+            if (page < 0 || page >= a.num_pages) {
+              flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
+              page = -1;
+            }
+          }
+        }
+        const unsigned load = __ballot_sync(0xffffffffu, lane < kUnitPages && page >= 0);
+        if (lane == 0) {
+          raw_valid[rs] = load;
+          raw_armed[rs] = static_cast<int32_t>(g);
+          mbar_arrive_expect_tx(bar(V_RAW_FULL + rs), __popc(load) * kRecBytesV);
+        }
+        __syncwarp();
+        if (lane < kUnitPages && page >= 0)
+          tma_load_2d(smem + kRawOff + rs * kRawStage + lane * kRawPage, &tmap, 0, (page * a.hkv + pc.h) * 36,
+                      bar(V_RAW_FULL + rs), policy);
+      }
+    }
+    if (!ok && lane == 0) {
+      // loads still landing complete before the CTA exits (fixed bound)
+      const int64_t first = g > kRawStages ? g - kRawStages : 0;
+      for (int64_t i = first; i <= g; ++i)
+        if (raw_armed[i % kRawStages] == static_cast<int32_t>(i))
+          mbar_wait(bar(V_RAW_FULL + static_cast<int>(i % kRawStages)), par(i, kRawStages));
+    }
+  } else if (warp >= kKWarp0 && warp < kKWarp0 + 4) {
+    // -------------------------------------------------------- K widening
+    // thread = key 32 q + lane of the unit (page key / 16, slot key % 16):
+    // its 256 dims, two fp16 per TMEM column, into lane 32 q + lane of the K
+    // stage; keys past the sequence or in a page that was not loaded are 0
+    const int q = warp - kKWarp0;
+    const int key = 32 * q + lane, pg = key >> 4, slot = key & 15;
+    int64_t g = 0;
+    bool ok = true;
+    while (ok && walk.next(a, &pc)) {
+      for (int k = 0; k < pc.n && ok; ++k, ++g) {
+        const int rs = static_cast<int>(g % kRawStages), kb = static_cast<int>(g & 1);
+        ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) && (g < 2 || waitw(V_K_FREE + kb, par(g - 2, 2)));
+        if (!ok) break;
+        const bool live = ((raw_valid[rs] >> pg) & 1) && (pc.p0 + k) * kUnitKeys + key < pc.s.len;
+        const uint32_t rec = smem_addr(smem + kRawOff + rs * kRawStage + pg * kRawPage);
+        uint4 sc = make_uint4(0, 0, 0, 0);
+        if (live) sc = lds128(rec + swz128(16 + (slot >> 3), (slot & 7) * 16));
+        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+        const uint32_t taddr = lane_base(tmem, q) + kTK + kb * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: dims 32c .. 32c + 31 (blocks 2c, 2c + 1)
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (live) w = lds128(rec + swz128(slot, 16 * c));
+          const uint32_t sb = (scw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;  // the two blocks' scale bytes
+          const uint32_t s2 = e4m3x2_to_f16x2(sb);
+          const uint32_t s_lo = prmt(s2, s2, 0x1010u), s_hi = prmt(s2, s2, 0x3232u);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          uint32_t h[16];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint32_t o4[4];
+            e2m1x8_unpack(ws[e], o4);
+            const uint32_t s = e < 2 ? s_lo : s_hi;
+#pragma unroll
+            for (int f = 0; f < 4; ++f) h[4 * e + f] = hmul2(o4[f], s);
+          }
+          tmem_st16(taddr + 16 * c, h);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(V_K_FULL + kb));
+          mbar_arrive(bar(V_RAW_EMPTY + rs));
+        }
+      }
+    }
+  } else if (warp >= kVWarp0 && warp < kVWarp0 + 4) {
+    // -------------------------------------------------------- V widening
+    // thread = dims d0 = 32 q + lane and d1 = 128 + d0 (TMEM lane 32 q + lane
+    // of the V^T halves): per page and slot pair, one code byte -> the fp16
+    // pair of the two keys -> one TMEM column.  The warp first transposes
+    // its four 16-dim blocks' scale bytes of the unit's 8 pages into a
+    // scratch [page][block][slot]; slots past the sequence scale to 0.
+    const int q = warp - kVWarp0;
+    const uint32_t scr = smem_addr(smem + kScrOff + q * kScrWarp);
+    int64_t g = 0;
+    bool ok = true;
+    while (ok && walk.next(a, &pc)) {
+      for (int k = 0; k < pc.n && ok; ++k, ++g) {
+        const int rs = static_cast<int>(g % kRawStages);
+        ok = waitw(V_RAW_FULL + rs, par(g, kRawStages));
+        if (!ok) break;
+        const uint32_t valid = raw_valid[rs];
+        const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStage);
+        const int key0 = (pc.p0 + k) * kUnitKeys;
+        {
+          // 512 scale bytes: the warp's blocks 2q, 2q + 1, 8 + 2q, 9 + 2q
+          // (index bi = 0 .. 3) of 16 slots of 8 pages.  Step it reads page
+          // it / 2, blocks bi = 2 (it % 2) + lane / 16, slot lane % 16: one
+          // page's two scale rows per instruction (at most a 2-way conflict)
+          const int sl = lane & 15;
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int j = it >> 1, bi = ((it & 1) << 1) | (lane >> 4);
+            const int blk = (bi >> 1) * 8 + 2 * q + (bi & 1);
+            const bool live = ((valid >> j) & 1) && key0 + 16 * j + sl < pc.s.len;
+            const uint32_t b = live ? lds8(raw + j * kRawPage + swz128(34 + (sl >> 3), (sl & 7) * 16 + blk)) : 0u;
+            asm volatile("st.shared.u8 [%0], %1;" ::"r"(scr + (j * 4 + bi) * 16 + sl), "h"(static_cast<uint16_t>(b))
+                         : "memory");
+          }
+        }
+        __syncwarp();
+        // V^T stage free: the P.V of unit g - 1 has completed
+        if (g >= 1) ok = waitw(V_V_FREE, par(g - 1, 1));
+        if (!ok) break;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          const int d = 128 * hh + 32 * q + lane;
+          const int bi = 2 * hh + (lane >> 4);  // block (d / 16) among the warp's four
+          uint32_t col[16];
+#pragma unroll 1
+          for (int j2 = 0; j2 < kUnitPages; j2 += 2) {  // two pages = 16 columns
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = j2 + jj;
+              const uint4 sc = lds128(scr + (j * 4 + bi) * 16);
+              uint32_t sf[8];  // fp16x2 scales of slot pairs 0 .. 7
+              e4m3x4_to_f16x2x2(sc.x, sf[0], sf[1]);
+              e4m3x4_to_f16x2x2(sc.y, sf[2], sf[3]);
+              e4m3x4_to_f16x2x2(sc.z, sf[4], sf[5]);
+              e4m3x4_to_f16x2x2(sc.w, sf[6], sf[7]);
+              const bool pv = (valid >> j) & 1;
+              const uint32_t rec = raw + j * kRawPage;
+#pragma unroll
+              for (int pr = 0; pr < 8; ++pr) {
+                const uint32_t code = pv ? lds8(rec + swz128(18 + 2 * pr + hh, d & 127)) : 0u;
+                col[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code), sf[pr]);
+              }
+            }
+            tmem_st16(lane_base(tmem, q) + kTV + 64 * hh + 8 * j2, col);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(V_V_FULL));
+          mbar_arrive(bar(V_RAW_EMPTY + rs));
+        }
+      }
+    }
+  } else if (warp == kQkWarp || warp == kPvWarp) {
+    // --------------------------------------------------------------- MMA
+    // QK and P.V from threads of different warps, so a wait of one never
+    // stalls the other's queue of products.
+    if (lane == 0) {
+      const bool qk = warp == kQkWarp;
+      const uint32_t idesc = idesc_f16(128, kRowsN);
+      int64_t g = 0, npiece = 0;
+      bool ok = true, issued = false;
+      while (ok && walk.next(a, &pc)) {
+        if (qk) ok = wait1(V_Q_FULL, static_cast<uint32_t>(npiece & 1));
+        for (int k = 0; ok && k < pc.n; ++k, ++g) {
+          if (qk) {
+            const int kb = static_cast<int>(g & 1), sb = kb;
+            ok = wait1(V_K_FULL + kb, par(g, 2)) && (g < 2 || wait1(V_S_FREE + sb, par(g - 2, 2)));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t q_base = smem_addr(smem + kQOff);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)  // 16 dims: 8 TMEM columns of K, 2 core matrices of Q^T
+              umma_f16_ta(tmem + kTS + 32 * sb, tmem + kTK + 128 * kb + 8 * kk,
+                          smem_desc(q_base + 256 * kk, 128, 4096), idesc, kk > 0);
+            umma_commit(bar(V_S_FULL + sb));
+            umma_commit(bar(V_K_FREE + kb));
+          } else {
+            const int pb = static_cast<int>(g % kPStages);
+            ok = wait1(V_V_FULL, par(g, 1)) && wait1(V_P_FULL + pb, par(g, kPStages));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_base = smem_addr(smem + kPOff + pb * kPBytes);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of V^T, 2 core matrices of P^T
+                umma_f16_ta(tmem + kTO + 32 * hh, tmem + kTV + 64 * hh + 8 * kk,
+                            smem_desc(p_base + 2 * kPLbo * kk, kPLbo, kPSbo), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(bar(V_V_FREE));
+            umma_commit(bar(V_PV_DONE + pb));
+          }
+          issued = true;
+        }
+        ++npiece;
+      }
+      // every issued product completes before TMEM is released (fixed bound)
+      if (issued)
+        umma_commit(bar(V_FINAL));
+      else
+        mbar_arrive(bar(V_FINAL));
+      mbar_wait(bar(V_FINAL), 0);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- softmax
+    // thread = key 32 q + lane of the unit (TMEM lane); columns = rows.  The
+    // four warps meet at named barrier 1 at fixed points, exchanging their
+    // state there, so that all of them take the same branch and stop
+    // together (a warp whose wait gave up carries on to the next meeting).
+    const int q = warp;
+    const int key = 32 * q + lane;
+    float* mref = reinterpret_cast<float*>(smem + kMrefOff);
+    int* lim = reinterpret_cast<int*>(smem + kLimOff);
+    float* alpha = reinterpret_cast<float*>(smem + kAlphaOff);
+    float* xchg = reinterpret_cast<float*>(smem + kXchgOff);
+    volatile uint32_t* flags = reinterpret_cast<uint32_t*>(smem + kFlagOff);
+    const uint32_t lb = lane_base(tmem, q);
+    // meeting: every warp posts bits, all read the OR and the AND
+    auto meet = [&](uint32_t bits, uint32_t* all_and, uint32_t* any_or) {
+      if (lane == 0) flags[q] = bits;
+      named_bar_sync(1, 128);
+      const uint32_t f0 = flags[0], f1 = flags[1], f2 = flags[2], f3 = flags[3];
+      named_bar_sync(1, 128);  // all have read before the next post
+      *all_and = f0 & f1 & f2 & f3;
+      *any_or = f0 | f1 | f2 | f3;
+    };
+    int64_t g = 0;
+    bool ok = true;
+    uint32_t all_and, any_or;
+    while (walk.next(a, &pc)) {
+      meet(ok ? 1u : 0u, &all_and, &any_or);
+      if (!(all_and & 1u)) break;
+      const int rows = a.group * pc.s.qlen;
+      // Q^T of the piece (B of QK): thread t: row t / 4, dims 64 (t % 4) ..
+      // + 63, fp16, core-matrix layout [32 rows][256 dims]; rows past the
+      // piece's are zero.  (Every QK of the previous piece has completed: its
+      // S were all read.)
+      {
+        const int t = threadIdx.x, r = t >> 2, d0 = 64 * (t & 3);
+        const bool live = r < rows;
+        const uint4* src = live ? reinterpret_cast<const uint4*>(
+                                      a.q + (static_cast<int64_t>(pc.s.q0 + r / a.group) * a.hq + pc.h * a.group +
+                                             r % a.group) * 256 + d0)
+                                : nullptr;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          uint32_t h[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            h[e] = f32x2_to_f16x2(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xFFFF0000u));
+          *reinterpret_cast<uint4*>(smem + kQOff + core_off(r, d0 + 8 * c, 256)) = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        fence_proxy_async();
+      }
+      if (threadIdx.x < kRowsN) {
+        const int r = threadIdx.x;
+        mref[r] = -INFINITY;
+        lim[r] = r < rows ? (a.causal ? pc.s.len - pc.s.qlen + r / a.group + 1 : pc.s.len) : 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(V_Q_FULL));
+      named_bar_sync(1, 128);  // mref and lim written
+      float l[kRowsN];
+#pragma unroll
+      for (int r = 0; r < kRowsN; ++r) l[r] = 0.f;
+
+      for (int k = 0; k < pc.n; ++k, ++g) {
+        const int sb = static_cast<int>(g & 1), pb = static_cast<int>(g % kPStages);
+        float x[kRowsN];
+        bool viol = false;
+        const int kg = (pc.p0 + k) * kUnitKeys + key;
+        // S^T column r of this key -> masked, scaled logits x (log2 units);
+        // the S slot is released at the end of the unit, so it can be read
+        // again after a reduction
+        auto load_x = [&]() {
+          uint32_t sr[kRowsN];
+          tmem_ld32(lb + kTS + 32 * sb, sr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < kRowsN; ++r) x[r] = kg < lim[r] ? __uint_as_float(sr[r]) * a.qk_scale_log2 : -INFINITY;
+        };
+        if (ok) ok = waitw(V_S_FULL + sb, par(g, 2));
+        if (ok) {
+          tc_fence_after();
+          load_x();
+#pragma unroll
+          for (int r = 0; r < kRowsN; ++r) viol |= x[r] > mref[r] + kMoveThreshold;
+        }
+        meet((ok ? 1u : 0u) | (__any_sync(0xffffffffu, viol) ? 2u : 0u), &all_and, &any_or);
+        if (!(all_and & 1u)) {
+          ok = false;
+          break;
+        }
+        if (any_or & 2u) {
+          // some row's logits passed its reference: the unit's exact row
+          // maxima (warp transpose-reduction, then over the four warps) move
+          // the references that grew by more than the threshold
+          // (in place on x, which is read again from S^T afterwards)
+#pragma unroll
+          for (int s = 16; s >= 1; s >>= 1) {
+            const bool up = lane & s;
+#pragma unroll
+            for (int i = 0; i < s; ++i) {
+              const float send = up ? x[i] : x[i + s];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+              x[i] = fmaxf(up ? x[i + s] : x[i], recv);
+            }
+          }
+          xchg[q * 32 + lane] = x[0];  // the warp's maximum of row `lane`
+          load_x();
+          named_bar_sync(1, 128);
+          if (threadIdx.x < kRowsN) {
+            const int r = threadIdx.x;
+            const float bm = fmaxf(fmaxf(xchg[r], xchg[32 + r]), fmaxf(xchg[64 + r], xchg[96 + r]));
+            const float m0 = mref[r];
+            const bool move = bm > m0 + kMoveThreshold || (m0 == -INFINITY && bm > -INFINITY);
+            const float mn = move ? bm : m0;
+            alpha[r] = (move && m0 != -INFINITY) ? fast_exp2(m0 - mn) : 1.f;
+            mref[r] = mn;
+          }
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int r = 0; r < kRowsN; ++r) l[r] *= alpha[r];
+          if (k > 0) {
+            // O^T (lane = dim, column = row) holds this piece's products up to
+            // unit g - 1: rescale its columns once that P.V has completed
+            ok = waitw(V_PV_DONE + static_cast<int>((g - 1) % kPStages), par(g - 1, kPStages));
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < 2 * kRowsN; c += 16) {  // both halves, 16 columns at a time
+                uint32_t o[16];
+                tmem_ld16(lb + kTO + c, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha[(c + e) & 31]);
+                tmem_st16(lb + kTO + c, o);
+              }
+              tmem_wait_st();
+              tc_fence_before();
+            }
+          }
+        }
+        if (!ok) continue;  // reported at the next meeting
+        // p = 2^(x - reference) (at most 2^threshold; 0 for masked keys)
+#pragma unroll
+        for (int r = 0; r < kRowsN; ++r) {
+          const float m = mref[r];
+          x[r] = fast_exp2(x[r] - (m == -INFINITY ? 0.f : m));
+          l[r] += x[r];
+        }
+        // P^T slot pb was last read by the P.V of unit g - kPStages
+        if (g >= kPStages) ok = waitw(V_PV_DONE + pb, par(g - kPStages, kPStages));
+        if (!ok) continue;
+        // P^T [32 rows][128 keys] fp16 (B of P.V): the lanes of a key pair
+        // swap halves so that the even key writes rows 0-15 and the odd key
+        // rows 16-31 as (even, odd) fp16 pairs; the padded core-matrix
+        // strides put a warp's 32 stores on distinct banks
+        {
+          uint8_t* pt = smem + kPOff + pb * kPBytes;
+          const int ke = key & ~1;
+          const bool odd = lane & 1;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float send = odd ? x[j] : x[16 + j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int r = odd ? 16 + j : j;
+            const uint32_t w = odd ? f32x2_to_f16x2(recv, x[16 + j]) : f32x2_to_f16x2(x[j], recv);
+            *reinterpret_cast<uint32_t*>(pt + p_off(r, ke)) = w;
+          }
+          fence_proxy_async();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(V_P_FULL + pb));
+            mbar_arrive(bar(V_S_FREE + sb));
+          }
+        }
+      }
+      if (!(all_and & 1u)) break;
+      // ---- end of the piece: the last P.V, the row sums, the partial
+      if (ok) ok = waitw(V_PV_DONE + static_cast<int>((g - 1) % kPStages), par(g - 1, kPStages));
+      {
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) {
+          const bool up = lane & s;
+#pragma unroll
+          for (int i = 0; i < s; ++i) {
+            const float send = up ? l[i] : l[i + s];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            l[i] = (up ? l[i + s] : l[i]) + recv;
+          }
+        }
+        xchg[q * 32 + lane] = l[0];  // the warp's sum of row `lane`
+      }
+      meet(ok ? 1u : 0u, &all_and, &any_or);
+      if (!(all_and & 1u)) break;
+      if (threadIdx.x < kRowsN) {
+        const int r = threadIdx.x;
+        alpha[r] = (xchg[r] + xchg[32 + r]) + (xchg[64 + r] + xchg[96 + r]);  // the row's sum L
+      }
+      named_bar_sync(1, 128);
+      const int64_t slot = pc.b * static_cast<int64_t>(a.hkv) + pc.h + blockIdx.x;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 2 * kRowsN; c += 16) {  // both halves, 16 rows at a time
+        uint32_t o[16];
+        tmem_ld16(lb + kTO + c, o);
+        tmem_wait_ld();
+        const int d = 128 * (c >> 5) + key;  // this lane's dim
+        if (slot < a.part_slots) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int r = (c + e) & 31;
+            if (r < rows) {
+              const float L = alpha[r];
+              a.o_part[(slot * a.rows_per_slot + r) * 256 + d] =
+                  L > 0.f ? __uint_as_float(o[e]) * (a.out_scale / L) : 0.f;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      if (threadIdx.x < kRowsN && threadIdx.x < rows && slot < a.part_slots) {
+        const int r = threadIdx.x;
+        const float L = alpha[r];
+        a.lse_part[slot * a.rows_per_slot + r] = L > 0.f ? (mref[r] + __log2f(L)) * kLn2V : -INFINITY;
+      }
+      // (alpha and mref are rewritten only after the next piece's meeting)
+    }
+  }
+
+  __syncthreads();
+  if (warp == kQkWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemColsV) : "memory");
+  }
+}
+
+}  // namespace
+
+// Launch the tensor-core verify tile (NVFP4 pools, 9 .. 32 query rows per KV
+// head); `map` is the pool's whole-record tensor map.
+int launch_verify(const CUtensorMap& map, const DecodeArgs& a, int grid, cudaStream_t stream) {
+  static std::atomic<uint64_t> configured{0};  // devices whose attribute is set
+  const int st = set_smem_limit_once(configured, reinterpret_cast<const void*>(verify_tile_kernel), kSmemV);
+  if (st != PNKV_OK) return st;
+  return launch_pdl(verify_tile_kernel, dim3(grid), dim3(kThreadsV), kSmemV, stream, map, a);
+}
+
+}  // namespace pnkv

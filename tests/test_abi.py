@@ -144,3 +144,25 @@ def test_decode_and_combine_validation(lib):
                                 None, None) == -1
     assert lib.split_kv_combine(P(256), P(256), P(256), P(256), 1, 0, 24, 4, 256, 1, P(256), 1,
                                 None, None) == 0
+
+
+def test_fp4q_prefill_validation(lib):
+    """paged_prefill_attention_fp4q refuses out-of-contract arguments and
+    requests it does not serve before touching the GPU."""
+    c = _cache()
+    P = ctypes.c_void_p
+
+    def call(cache=c, hq=24, max_qlen=20, q_scale=0.01, sm=0.0625, q=P(256)):
+        return lib.paged_prefill_attention_fp4q(ctypes.byref(cache), q, P(256), P(256), 4, P(256), 1, 20,
+                                                hq, max_qlen, sm, 1, q_scale, P(256), P(256), 1000, P(256),
+                                                P(256), None)
+
+    for bad in (dict(q_scale=0.0), dict(q_scale=-1.0), dict(q_scale=float("inf")),
+                dict(q_scale=float("nan")), dict(q_scale=2.0 ** -110), dict(q_scale=2.0 ** 110),
+                dict(sm=0.0), dict(hq=25), dict(q=None), dict(max_qlen=0)):
+        assert call(**bad) == _lib.PNKV_ERR_INVALID_ARG, bad
+    # at most 64 rows per KV head (6 x 10) is a decode step, not a prefill chunk
+    assert call(max_qlen=10) == _lib.PNKV_ERR_UNSUPPORTED
+    # only NVFP4 pools hold codes the block-scaled product can read
+    for dtype in (0, 2, 3):
+        assert call(cache=_cache(dtype=dtype)) == _lib.PNKV_ERR_UNSUPPORTED, dtype

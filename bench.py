@@ -370,17 +370,29 @@ def is_tile_path(w):
     return int(w.qlen.max()) * (w.num_q_heads // w.num_kv_heads) > 64
 
 
-def roofline_of(w, decode_ms):
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # dense tensor rates of GB300, nominal
+
+
+def roofline_of(w, decode_ms, fp4q=False):
     """Roofline of the step's dominant kernel: HBM bytes of KV + scales for
-    the split-KV decode, causal-exact QK^T + PV FLOPs for the tensor-core tile."""
+    the split-KV decode, causal-exact QK^T + PV FLOPs for the tensor-core tile.
+    With NVFP4 queries half of the FLOPs (QK^T) run at the FP4 rate and half
+    (P V) at the fp16 rate; the peak is then the harmonic combination of the
+    two rates, the FP4 one taken as the measured bf16 peak times the nominal
+    FP4 / bf16 ratio."""
     keys = int(w.seq_lens.sum())
     if is_tile_path(w):
         flops = attention_flops(w)
         tflops = flops / (decode_ms * 1e-3) / 1e12
         tpeak, tkind = tensor_peak()
+        kernel = "prefill_tile_kernel (tcgen05, kind::f16)"
+        if fp4q:
+            tpeak = 2.0 / (1.0 / (tpeak * NOMINAL_FP4_OVER_BF16) + 1.0 / tpeak)
+            tkind += " (QK^T at bf16 x 13.5/2.25, P V at bf16)"
+            kernel = "prefill_tile_kernel (tcgen05, kind::mxf4nvf4 QK^T + kind::f16 P V)"
         return {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": tflops / tpeak, "traffic": None, "peak_kind": tkind,
-                "kernel": "prefill_tile_kernel (tcgen05)", "algorithmic_flops_per_launch": flops}
+                "kernel": kernel, "algorithmic_flops_per_launch": flops}
     peak, peak_kind = peaks()
     algo_bytes = keys * ALGO_BYTES_PER_TOKEN[w.kv_dtype]
     achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
@@ -406,7 +418,7 @@ def config_record(cfg, K, W, local, fp4q=False):
     pool_bytes = s.cache.pool.numel()
     flush = l2_flusher(torch) if pool_bytes < (256 << 20) else None
     m = measure_steps(s, K, W, stream, local, flush, q_scale=w.g_q if fp4q else None)
-    roof = roofline_of(w, m["decode_ms"])
+    roof = roofline_of(w, m["decode_ms"], fp4q)
     keys = int(w.seq_lens.sum())
     rec = {"workload": w.name + (", NVFP4 queries (block-scaled FP4 QK^T)" if fp4q else ""),
            "kv_dtype": w.kv_dtype, "keys": keys,
@@ -491,7 +503,7 @@ def run_ours(args):
     e2e_value = replica_rate(keys, e2e_ms, world)
     err = s.error_word()
 
-    roofline = roofline_of(w, m["decode_ms"])
+    roofline = roofline_of(w, m["decode_ms"], qs is not None)
     tile_path = is_tile_path(w)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,

@@ -38,3 +38,19 @@ def test_chunked_prefill_flops():
     f = bench.attention_flops(w)
     assert f == (1040384 * 8192 + 8192 * 8193 // 2) * 24 * 256 * 4
     assert round(f / 1e14, 2) == 2.10
+
+
+def test_fp4q_tile_peak_is_the_harmonic_mix():
+    """With NVFP4 queries the FLOPs split evenly between a block-scaled FP4
+    QK^T and an fp16 P V: the peak is the rate at which that mix runs, i.e.
+    the harmonic combination of the two rates (FP4 = bf16 x 13.5 / 2.25)."""
+    w = SimpleNamespace(batch=1, seq_lens=np.array([1040384 + 8192]), qlen=np.array([8192]),
+                        causal=1, num_q_heads=24, num_kv_heads=4, head_dim=256, kv_dtype="nvfp4")
+    f16 = bench.roofline_of(w, 100.0)
+    fp4 = bench.roofline_of(w, 100.0, fp4q=True)
+    p = f16["peak"]
+    assert abs(fp4["peak"] - 2.0 / (1.0 / (6.0 * p) + 1.0 / p)) < 1e-9 * p
+    # half of the work at the f16 rate alone takes half the f16 time, the
+    # other half a sixth of that: the mix runs at 12/7 of the f16 rate
+    assert abs(fp4["peak"] / p - 12.0 / 7.0) < 1e-12
+    assert fp4["achieved"] == f16["achieved"]

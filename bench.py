@@ -145,6 +145,9 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+DECODE_SOURCES = ("decode.cu", "decode_common.cuh", "device_common.cuh")
+
+
 def profiled_traffic(kv_dtype):
     """DRAM bytes per decode launch from the committed ncu summary, or None when
     the decode kernel's source changed since that capture."""
@@ -161,7 +164,7 @@ def profiled_traffic(kv_dtype):
             if line.startswith(key):
                 vals[key] = line.split(":", 1)[1].strip()
     src = b"".join(open(os.path.join(ROOT, "paged_nvfp4_kv_gb300", "csrc", f), "rb").read()
-                   for f in ("decode.cu", "device_common.cuh"))
+                   for f in DECODE_SOURCES)
     if hashlib.sha256(src).hexdigest()[:16] != vals.get("source_sha256_16:"):
         return None
     return int(vals["traffic_bytes_per_launch:"])

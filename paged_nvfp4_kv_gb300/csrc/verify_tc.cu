@@ -79,7 +79,9 @@ constexpr int kPBytes = 4 * kPSbo;
 constexpr int kScrOff = kPOff + kPStages * kPBytes;      // per V warp: scales [page][4 blocks][16 slots]
 constexpr int kScrWarp = kUnitPages * 4 * 16;
 constexpr int kMrefOff = kScrOff + 4 * kScrWarp;         // float [32]: per-row reference maximum (log2)
-constexpr int kLimOff = kMrefOff + kRowsN * 4;           // int [32]: keys row r may see
+constexpr int kThrOff = kMrefOff + kRowsN * 4;           // float [32]: reference + threshold
+constexpr int kBaseOff = kThrOff + kRowsN * 4;           // float [32]: exponent base (reference, 0 if none)
+constexpr int kLimOff = kBaseOff + kRowsN * 4;           // int [32]: keys row r may see
 constexpr int kAlphaOff = kLimOff + kRowsN * 4;          // float [32]: rescale factors
 constexpr int kXchgOff = kAlphaOff + kRowsN * 4;         // float [4 warps][32]: reductions
 constexpr int kFlagOff = kXchgOff + 4 * kRowsN * 4;      // uint [4]: softmax warps' flags
@@ -276,6 +278,10 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // stage; keys past the sequence or in a page that was not loaded are 0
     const int q = warp - kKWarp0;
     const int key = 32 * q + lane, pg = key >> 4, slot = key & 15;
+    uint32_t kswz[8];  // the slot's row with its 16-byte chunks swizzled
+#pragma unroll
+    for (int c = 0; c < 8; ++c) kswz[c] = pg * kRawPage + swz128(slot, 16 * c);
+    const uint32_t kscale = pg * kRawPage + swz128(16 + (slot >> 3), (slot & 7) * 16);
     int64_t g = 0;
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
@@ -284,15 +290,15 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) && (g < 2 || waitw(V_K_FREE + kb, par(g - 2, 2)));
         if (!ok) break;
         const bool live = ((raw_valid[rs] >> pg) & 1) && (pc.p0 + k) * kUnitKeys + key < pc.s.len;
-        const uint32_t rec = smem_addr(smem + kRawOff + rs * kRawStage + pg * kRawPage);
+        const uint32_t rawb = smem_addr(smem + kRawOff + rs * kRawStage);
         uint4 sc = make_uint4(0, 0, 0, 0);
-        if (live) sc = lds128(rec + swz128(16 + (slot >> 3), (slot & 7) * 16));
+        if (live) sc = lds128(rawb + kscale);
         const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
         const uint32_t taddr = lane_base(tmem, q) + kTK + kb * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: dims 32c .. 32c + 31 (blocks 2c, 2c + 1)
           uint4 w = make_uint4(0, 0, 0, 0);
-          if (live) w = lds128(rec + swz128(slot, 16 * c));
+          if (live) w = lds128(rawb + kswz[c]);
           const uint32_t sb = (scw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;  // the two blocks' scale bytes
           const uint32_t s2 = e4m3x2_to_f16x2(sb);
           const uint32_t s_lo = prmt(s2, s2, 0x1010u), s_hi = prmt(s2, s2, 0x3232u);
@@ -324,8 +330,29 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // pair of the two keys -> one TMEM column.  The warp first transposes
     // its four 16-dim blocks' scale bytes of the unit's 8 pages into a
     // scratch [page][block][slot]; slots past the sequence scale to 0.
+    // Every raw row index below is a compile-time constant, so each byte
+    // load is one instruction: the thread keeps its column's 8 swizzled
+    // offsets (the 16-byte chunk of the column XOR the row's residue mod 8).
     const int q = warp - kVWarp0;
     const uint32_t scr = smem_addr(smem + kScrOff + q * kScrWarp);
+    const uint32_t col = 32 * q + lane;  // byte of a 128-byte half-row: d & 127
+    uint32_t swz[8];
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) swz[c8] = ((((col >> 4) ^ c8) & 7) << 4) | (col & 15);
+    // scratch fill: step it reads page it / 2, block index bi = 2 (it % 2) +
+    // lane / 16 (blocks 2q, 2q + 1, 8 + 2q, 9 + 2q), slot lane % 16: one
+    // page's two scale rows per instruction (at most a 2-way conflict)
+    const int sl = lane & 15;
+    const uint32_t srow = 34 + (sl >> 3);  // raw row of the slot's scales
+    uint32_t sfill[2];
+#pragma unroll
+    for (int par2 = 0; par2 < 2; ++par2) {
+      const int bi = (par2 << 1) | (lane >> 4);
+      const int blk = (bi >> 1) * 8 + 2 * q + (bi & 1);
+      sfill[par2] = swz128(srow, (sl & 7) * 16 + blk);
+    }
+    const uint32_t sdst = scr + sl + 16 * (lane >> 4);  // + (4 j + 2 (it % 2)) * 16
+    const uint32_t sread = scr + 16 * (lane >> 4);      // + (4 j + 2 hh) * 16
     int64_t g = 0;
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
@@ -335,52 +362,45 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (!ok) break;
         const uint32_t valid = raw_valid[rs];
         const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStage);
-        const int key0 = (pc.p0 + k) * kUnitKeys;
-        {
-          // 512 scale bytes: the warp's blocks 2q, 2q + 1, 8 + 2q, 9 + 2q
-          // (index bi = 0 .. 3) of 16 slots of 8 pages.  Step it reads page
-          // it / 2, blocks bi = 2 (it % 2) + lane / 16, slot lane % 16: one
-          // page's two scale rows per instruction (at most a 2-way conflict)
-          const int sl = lane & 15;
-#pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int j = it >> 1, bi = ((it & 1) << 1) | (lane >> 4);
-            const int blk = (bi >> 1) * 8 + 2 * q + (bi & 1);
-            const bool live = ((valid >> j) & 1) && key0 + 16 * j + sl < pc.s.len;
-            const uint32_t b = live ? lds8(raw + j * kRawPage + swz128(34 + (sl >> 3), (sl & 7) * 16 + blk)) : 0u;
-            asm volatile("st.shared.u8 [%0], %1;" ::"r"(scr + (j * 4 + bi) * 16 + sl), "h"(static_cast<uint16_t>(b))
-                         : "memory");
-          }
+        const int keys_left = pc.s.len - (pc.p0 + k) * kUnitKeys;  // keys of the unit in the sequence
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+          const int j = it >> 1;
+          const bool live = ((valid >> j) & 1) && 16 * j + sl < keys_left;
+          const uint32_t b = live ? lds8(raw + j * kRawPage + sfill[it & 1]) : 0u;
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(sdst + (4 * j + 2 * (it & 1)) * 16), "h"(static_cast<uint16_t>(b))
+                       : "memory");
         }
         __syncwarp();
         // V^T stage free: the P.V of unit g - 1 has completed
         if (g >= 1) ok = waitw(V_V_FREE, par(g - 1, 1));
         if (!ok) break;
-#pragma unroll 1
+        uint32_t base[8];  // raw + this thread's swizzled column for each row residue
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) base[c8] = raw + swz[c8];
+#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int d = 128 * hh + 32 * q + lane;
-          const int bi = 2 * hh + (lane >> 4);  // block (d / 16) among the warp's four
-          uint32_t col[16];
-#pragma unroll 1
+#pragma unroll
           for (int j2 = 0; j2 < kUnitPages; j2 += 2) {  // two pages = 16 columns
+            uint32_t colw[16];
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
               const int j = j2 + jj;
-              const uint4 sc = lds128(scr + (j * 4 + bi) * 16);
-              uint32_t sf[8];  // fp16x2 scales of slot pairs 0 .. 7
+              const uint4 sc = lds128(sread + (4 * j + 2 * hh) * 16);
+              uint32_t sf[8];  // fp16x2 scales of slot pairs 0 .. 7 (zero past the sequence)
               e4m3x4_to_f16x2x2(sc.x, sf[0], sf[1]);
               e4m3x4_to_f16x2x2(sc.y, sf[2], sf[3]);
               e4m3x4_to_f16x2x2(sc.z, sf[4], sf[5]);
               e4m3x4_to_f16x2x2(sc.w, sf[6], sf[7]);
               const bool pv = (valid >> j) & 1;
-              const uint32_t rec = raw + j * kRawPage;
 #pragma unroll
               for (int pr = 0; pr < 8; ++pr) {
-                const uint32_t code = pv ? lds8(rec + swz128(18 + 2 * pr + hh, d & 127)) : 0u;
-                col[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code), sf[pr]);
+                const int row = 18 + 2 * pr + hh;  // compile-time
+                const uint32_t code = pv ? lds8(base[row & 7] + j * kRawPage + row * 128) : 0u;
+                colw[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code), sf[pr]);
               }
             }
-            tmem_st16(lane_base(tmem, q) + kTV + 64 * hh + 8 * j2, col);
+            tmem_st16(lane_base(tmem, q) + kTV + 64 * hh + 8 * j2, colw);
           }
         }
         tmem_wait_st();
@@ -452,6 +472,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     const int q = warp;
     const int key = 32 * q + lane;
     float* mref = reinterpret_cast<float*>(smem + kMrefOff);
+    float* thr = reinterpret_cast<float*>(smem + kThrOff);
+    float* basev = reinterpret_cast<float*>(smem + kBaseOff);
     int* lim = reinterpret_cast<int*>(smem + kLimOff);
     float* alpha = reinterpret_cast<float*>(smem + kAlphaOff);
     float* xchg = reinterpret_cast<float*>(smem + kXchgOff);
@@ -499,8 +521,13 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       if (threadIdx.x < kRowsN) {
         const int r = threadIdx.x;
         mref[r] = -INFINITY;
+        thr[r] = -INFINITY;
+        basev[r] = 0.f;
         lim[r] = r < rows ? (a.causal ? pc.s.len - pc.s.qlen + r / a.group + 1 : pc.s.len) : 0;
       }
+      // keys every query row of the piece sees: a unit below this needs no
+      // mask (its rows past the piece's carry harmless values, never written)
+      const int vis_all = a.causal ? pc.s.len - pc.s.qlen + 1 : pc.s.len;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(V_Q_FULL));
       named_bar_sync(1, 128);  // mref and lim written
@@ -516,19 +543,36 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         // S^T column r of this key -> masked, scaled logits x (log2 units);
         // the S slot is released at the end of the unit, so it can be read
         // again after a reduction
+        const bool unmasked = (pc.p0 + k + 1) * kUnitKeys <= vis_all;  // uniform over the CTA
         auto load_x = [&]() {
           uint32_t sr[kRowsN];
           tmem_ld32(lb + kTS + 32 * sb, sr);
           tmem_wait_ld();
+          if (unmasked) {
 #pragma unroll
-          for (int r = 0; r < kRowsN; ++r) x[r] = kg < lim[r] ? __uint_as_float(sr[r]) * a.qk_scale_log2 : -INFINITY;
+            for (int r = 0; r < kRowsN; ++r) x[r] = __uint_as_float(sr[r]) * a.qk_scale_log2;
+          } else {
+#pragma unroll
+            for (int r4 = 0; r4 < kRowsN; r4 += 4) {
+              const int4 l4 = *reinterpret_cast<const int4*>(lim + r4);
+              const int lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                x[r4 + e] = kg < lv[e] ? __uint_as_float(sr[r4 + e]) * a.qk_scale_log2 : -INFINITY;
+            }
+          }
         };
         if (ok) ok = waitw(V_S_FULL + sb, par(g, 2));
         if (ok) {
           tc_fence_after();
           load_x();
+          float over = -INFINITY;  // max over rows of (x - reference - threshold)
 #pragma unroll
-          for (int r = 0; r < kRowsN; ++r) viol |= x[r] > mref[r] + kMoveThreshold;
+          for (int r4 = 0; r4 < kRowsN; r4 += 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(thr + r4);
+            over = fmaxf(over, fmaxf(fmaxf(x[r4] - t4.x, x[r4 + 1] - t4.y), fmaxf(x[r4 + 2] - t4.z, x[r4 + 3] - t4.w)));
+          }
+          viol = over > 0.f;  // (x = -inf against thr = -inf gives NaN: no move)
         }
         meet((ok ? 1u : 0u) | (__any_sync(0xffffffffu, viol) ? 2u : 0u), &all_and, &any_or);
         if (!(all_and & 1u)) {
@@ -561,6 +605,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             const float mn = move ? bm : m0;
             alpha[r] = (move && m0 != -INFINITY) ? fast_exp2(m0 - mn) : 1.f;
             mref[r] = mn;
+            thr[r] = mn + kMoveThreshold;
+            basev[r] = mn == -INFINITY ? 0.f : mn;
           }
           named_bar_sync(1, 128);
 #pragma unroll
@@ -588,10 +634,14 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (!ok) continue;  // reported at the next meeting
         // p = 2^(x - reference) (at most 2^threshold; 0 for masked keys)
 #pragma unroll
-        for (int r = 0; r < kRowsN; ++r) {
-          const float m = mref[r];
-          x[r] = fast_exp2(x[r] - (m == -INFINITY ? 0.f : m));
-          l[r] += x[r];
+        for (int r4 = 0; r4 < kRowsN; r4 += 4) {
+          const float4 b4 = *reinterpret_cast<const float4*>(basev + r4);
+          const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[r4 + e] = fast_exp2(x[r4 + e] - bv[e]);
+            l[r4 + e] += x[r4 + e];
+          }
         }
         // P^T slot pb was last read by the P.V of unit g - kPStages
         if (g >= kPStages) ok = waitw(V_PV_DONE + pb, par(g - kPStages, kPStages));
@@ -601,16 +651,17 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         // rows 16-31 as (even, odd) fp16 pairs; the padded core-matrix
         // strides put a warp's 32 stores on distinct banks
         {
-          uint8_t* pt = smem + kPOff + pb * kPBytes;
           const int ke = key & ~1;
           const bool odd = lane & 1;
+          // rows j (even key) or 16 + j (odd key): thread-constant base plus a
+          // compile-time offset per j
+          uint8_t* pt = smem + kPOff + pb * kPBytes + p_off(odd ? 16 : 0, ke);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float send = odd ? x[j] : x[16 + j];
             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const int r = odd ? 16 + j : j;
-            const uint32_t w = odd ? f32x2_to_f16x2(recv, x[16 + j]) : f32x2_to_f16x2(x[j], recv);
-            *reinterpret_cast<uint32_t*>(pt + p_off(r, ke)) = w;
+            const float lo = odd ? recv : x[j], hi = odd ? x[16 + j] : recv;
+            *reinterpret_cast<uint32_t*>(pt + (j >> 3) * kPSbo + (j & 7) * 16) = f32x2_to_f16x2(lo, hi);
           }
           fence_proxy_async();
           tc_fence_before();

@@ -501,15 +501,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           __syncwarp();
+          // all loads first (codes of the four pages, then their scales); the
+          // code rows 18 - kRawRow0 + d / 128 + 2 pr have residues mod 8 that
+          // repeat every 4 pairs, so 4 swizzled column offsets make each byte
+          // load one instruction
           const uint32_t code_row = 18 - P::kRawRow0 + (d >> 7), code_col = d & 127;
-          // all loads first (codes of the four pages, then their scales)
+          uint32_t cbase[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) cbase[m] = raw + swz128(code_row + 2 * m, code_col);
           uint32_t code[kBlockPages][8];
           uint4 sc[kBlockPages];
 #pragma unroll
           for (int pg = 0; pg < kBlockPages; ++pg) {
-            const uint32_t rec = raw + pg * P::kRawPageBytes;
 #pragma unroll
-            for (int pr = 0; pr < 8; ++pr) code[pg][pr] = lds8(rec + swz128(code_row + 2 * pr, code_col));
+            for (int pr = 0; pr < 8; ++pr)
+              code[pg][pr] = lds8(cbase[pr & 3] + pg * P::kRawPageBytes + (pr >> 2) * 8 * 128);
             sc[pg] = lds128(scr + pg * 32 + ((d >> 4) & 1) * 16);
           }
 #pragma unroll

@@ -89,11 +89,14 @@ constexpr int kBarOffV = (kFlagOff + 16 + 7) & ~7;
 enum {
   V_RAW_FULL = 0,
   V_RAW_EMPTY = V_RAW_FULL + kRawStages,
-  V_K_FULL = V_RAW_EMPTY + kRawStages,
-  V_K_FREE = V_K_FULL + 2,
-  V_V_FULL = V_K_FREE + 2,
-  V_V_FREE = V_V_FULL + 1,
-  V_S_FULL = V_V_FREE + 1,
+  // per slot and per role, so that each barrier has one producer and its
+  // phases come in order: K or V^T widened into the slot; the QK or P.V
+  // that read it completed
+  V_FULL_K = V_RAW_EMPTY + kRawStages,
+  V_FULL_V = V_FULL_K + 3,
+  V_FREE_K = V_FULL_V + 3,
+  V_FREE_V = V_FREE_K + 3,
+  V_S_FULL = V_FREE_V + 3,
   V_S_FREE = V_S_FULL + 2,
   V_P_FULL = V_S_FREE + 2,
   V_PV_DONE = V_P_FULL + kPStages,
@@ -106,10 +109,22 @@ constexpr int kSmemV = kMiscOffV + 64 + 1024;
 static_assert(kSmemV <= 232448, "verify tile shared memory plan too large");
 static_assert(kQOff % 1024 == 0, "raw ring slots need 1,024-byte alignment");
 
-// TMEM columns: K (two stages of 128), V^T (halves of 64), S^T (two stages
-// of 32), O^T (halves of 32)
+// TMEM columns: three 128-column slots that K and V^T take in turn (unit g's
+// K is allocation 2g, its V^T allocation 2g + 1, allocation a in slot a % 3;
+// V^T's halves at +0 and +64), then S^T (two stages of 32) and O^T (halves of
+// 32).  A slot is freed by the product that read it, so the V^T of unit g + 1
+// waits only for the QK of unit g, and the K of unit g + 1 for the P.V of
+// unit g - 1.
 constexpr uint32_t kTmemColsV = 512;
-constexpr uint32_t kTK = 0, kTV = 256, kTS = 384, kTO = 448;
+constexpr uint32_t kTS = 384, kTO = 448;
+
+// Slot of allocation a, and the parity of its phase on its role's barriers of
+// that slot: a slot's uses by one role are 6 allocations apart (K uses are
+// even, V^T uses odd, both in a fixed residue mod 3), so allocation a is that
+// role's use number a / 6 of the slot.  The previous user of a's slot is
+// allocation a - 3, of the other role.
+__device__ __forceinline__ int slot_of(int64_t a) { return static_cast<int>(a % 3); }
+__device__ __forceinline__ uint32_t use_parity(int64_t a) { return static_cast<uint32_t>((a / 6) & 1); }
 
 __device__ __forceinline__ uint64_t* vbar(uint8_t* smem, int i) {
   return reinterpret_cast<uint64_t*>(smem + kBarOffV) + i;
@@ -144,14 +159,16 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       mbar_init(bar(V_RAW_EMPTY + i), 8);  // the K and the V warps
       raw_armed[i] = -1;
     }
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bar(V_FULL_K + i), 4);
+      mbar_init(bar(V_FULL_V + i), 4);
+      mbar_init(bar(V_FREE_K + i), 1);
+      mbar_init(bar(V_FREE_V + i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(V_K_FULL + i), 4);
-      mbar_init(bar(V_K_FREE + i), 1);
       mbar_init(bar(V_S_FULL + i), 1);
       mbar_init(bar(V_S_FREE + i), 4);
     }
-    mbar_init(bar(V_V_FULL), 4);
-    mbar_init(bar(V_V_FREE), 1);
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(bar(V_P_FULL + i), 4);
       mbar_init(bar(V_PV_DONE + i), 1);
@@ -286,15 +303,18 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
       for (int k = 0; k < pc.n && ok; ++k, ++g) {
-        const int rs = static_cast<int>(g % kRawStages), kb = static_cast<int>(g & 1);
-        ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) && (g < 2 || waitw(V_K_FREE + kb, par(g - 2, 2)));
+        const int rs = static_cast<int>(g % kRawStages);
+        const int64_t al = 2 * g;  // this unit's K allocation
+        const int ks = slot_of(al);
+        // the slot's previous user is the V^T of unit g - 2 (allocation al - 3)
+        ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) && (al < 3 || waitw(V_FREE_V + ks, use_parity(al - 3)));
         if (!ok) break;
         const bool live = ((raw_valid[rs] >> pg) & 1) && (pc.p0 + k) * kUnitKeys + key < pc.s.len;
         const uint32_t rawb = smem_addr(smem + kRawOff + rs * kRawStage);
         uint4 sc = make_uint4(0, 0, 0, 0);
         if (live) sc = lds128(rawb + kscale);
         const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-        const uint32_t taddr = lane_base(tmem, q) + kTK + kb * 128;
+        const uint32_t taddr = lane_base(tmem, q) + 128 * ks;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: dims 32c .. 32c + 31 (blocks 2c, 2c + 1)
           uint4 w = make_uint4(0, 0, 0, 0);
@@ -318,7 +338,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar(V_K_FULL + kb));
+          mbar_arrive(bar(V_FULL_K + ks));
           mbar_arrive(bar(V_RAW_EMPTY + rs));
         }
       }
@@ -372,15 +392,18 @@ __global__ void __launch_bounds__(kThreadsV, 1)
                        : "memory");
         }
         __syncwarp();
-        // V^T stage free: the P.V of unit g - 1 has completed
-        if (g >= 1) ok = waitw(V_V_FREE, par(g - 1, 1));
+        // the slot of this unit's V^T (allocation 2g + 1) is free once the
+        // QK of unit g - 1 (allocation 2g - 2) has completed
+        const int64_t al = 2 * g + 1;
+        const int vs = slot_of(al);
+        if (al >= 3) ok = waitw(V_FREE_K + vs, use_parity(al - 3));
         if (!ok) break;
         uint32_t base[8];  // raw + this thread's swizzled column for each row residue
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) base[c8] = raw + swz[c8];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
+#pragma unroll 1
           for (int j2 = 0; j2 < kUnitPages; j2 += 2) {  // two pages = 16 columns
             uint32_t colw[16];
 #pragma unroll
@@ -400,14 +423,14 @@ __global__ void __launch_bounds__(kThreadsV, 1)
                 colw[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code), sf[pr]);
               }
             }
-            tmem_st16(lane_base(tmem, q) + kTV + 64 * hh + 8 * j2, colw);
+            tmem_st16(lane_base(tmem, q) + 128 * vs + 64 * hh + 8 * j2, colw);
           }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar(V_V_FULL));
+          mbar_arrive(bar(V_FULL_V + vs));
           mbar_arrive(bar(V_RAW_EMPTY + rs));
         }
       }
@@ -425,20 +448,24 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (qk) ok = wait1(V_Q_FULL, static_cast<uint32_t>(npiece & 1));
         for (int k = 0; ok && k < pc.n; ++k, ++g) {
           if (qk) {
-            const int kb = static_cast<int>(g & 1), sb = kb;
-            ok = wait1(V_K_FULL + kb, par(g, 2)) && (g < 2 || wait1(V_S_FREE + sb, par(g - 2, 2)));
+            const int sb = static_cast<int>(g & 1);
+            const int64_t al = 2 * g;  // K of unit g
+            const int ks = slot_of(al);
+            ok = wait1(V_FULL_K + ks, use_parity(al)) && (g < 2 || wait1(V_S_FREE + sb, par(g - 2, 2)));
             if (!ok) break;
             tc_fence_after();
             const uint32_t q_base = smem_addr(smem + kQOff);
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)  // 16 dims: 8 TMEM columns of K, 2 core matrices of Q^T
-              umma_f16_ta(tmem + kTS + 32 * sb, tmem + kTK + 128 * kb + 8 * kk,
+              umma_f16_ta(tmem + kTS + 32 * sb, tmem + 128 * ks + 8 * kk,
                           smem_desc(q_base + 256 * kk, 128, 4096), idesc, kk > 0);
             umma_commit(bar(V_S_FULL + sb));
-            umma_commit(bar(V_K_FREE + kb));
+            umma_commit(bar(V_FREE_K + ks));
           } else {
             const int pb = static_cast<int>(g % kPStages);
-            ok = wait1(V_V_FULL, par(g, 1)) && wait1(V_P_FULL + pb, par(g, kPStages));
+            const int64_t al = 2 * g + 1;  // V^T of unit g
+            const int vs = slot_of(al);
+            ok = wait1(V_FULL_V + vs, use_parity(al)) && wait1(V_P_FULL + pb, par(g, kPStages));
             if (!ok) break;
             tc_fence_after();
             const uint32_t p_base = smem_addr(smem + kPOff + pb * kPBytes);
@@ -446,9 +473,9 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of V^T, 2 core matrices of P^T
-                umma_f16_ta(tmem + kTO + 32 * hh, tmem + kTV + 64 * hh + 8 * kk,
+                umma_f16_ta(tmem + kTO + 32 * hh, tmem + 128 * vs + 64 * hh + 8 * kk,
                             smem_desc(p_base + 2 * kPLbo * kk, kPLbo, kPSbo), idesc, (k > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(bar(V_V_FREE));
+            umma_commit(bar(V_FREE_V + vs));
             umma_commit(bar(V_PV_DONE + pb));
           }
           issued = true;

@@ -234,6 +234,13 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return out;
 }
 
+// max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

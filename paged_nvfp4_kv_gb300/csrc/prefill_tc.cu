@@ -128,7 +128,7 @@ struct Layout {
   static constexpr int kQOff = kRawOff + P::kRawStages * kRawStageBytes;  // FP4 Q codes
   static constexpr int kSfaXOff = kQOff + P::kQBytes;
   static constexpr int kScrOff = kSfaXOff + P::kSfaXBytes;  // per dequant warp: V scales
-  static constexpr int kScrWarpBytes = kBlockPages * 32;   // [page][2 blocks][16 slots]
+  static constexpr int kScrWarpBytes = kBlockPages * 2 * 8 * 4;  // fp16x2 [page][2 blocks][8 slot pairs]
   static constexpr int kBarOff = kScrOff + kDequantWarps * kScrWarpBytes;
   // barriers, in this order
   static constexpr int B_RAW_FULL = 0;
@@ -481,23 +481,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // V^T: thread dt owns dim d = dt over the block's 64 keys.  The
         // lanes of a warp read consecutive code bytes of a slot-pair row, and
         // each quarter-warp stores one contiguous core matrix (8 dims x 8
-        // keys).  The block scales of the warp's two 16-dim blocks are first
-        // transposed through a per-warp scratch ([page][block][slot]), so a
-        // thread reads the 16 slot scales of its block with one 16-byte load.
-        // (Raw rows are record rows minus kRawRow0: V codes at record rows
-        // 18 .. 33, V scales at 34 and 35.)
+        // keys).  The block scales of the warp's two 16-dim blocks (each
+        // shared by 16 of its lanes) are first converted into a per-warp
+        // scratch of fp16 pairs [page][block][slot pair], so a thread reads
+        // the 8 pair scales of its block with two 16-byte loads.  Slots past
+        // the sequence and pages that were not loaded scale to 0, which
+        // zeroes their values whatever the stale codes.  (Raw rows are record
+        // rows minus kRawRow0: V codes at record rows 18 .. 33, V scales at
+        // 34 and 35, slot s's 16 block scales at byte 16 (s % 8) of row
+        // 34 + s / 8.)
         {
           const int d = dt;
           const int wq = dt >> 5;
           const uint32_t scr = smem_addr(smem + L::kScrOff + wq * L::kScrWarpBytes);
           {
-            const int slot = lane & 15, bsel = lane >> 4, blk = 2 * wq + bsel;
+            const int bsel = (lane >> 3) & 1, fp = lane & 7, blk = 2 * wq + bsel;
+            const uint32_t o0 = swz128(34 - P::kRawRow0 + (fp >> 2), ((2 * fp) & 7) * 16 + blk);
+            const uint32_t o1 = swz128(34 - P::kRawRow0 + (fp >> 2), ((2 * fp + 1) & 7) * 16 + blk);
+            const int keys_left = t.len - (t.kb0 + j) * kBlockKeys;  // keys of the block in the sequence
+            uint32_t* fdst = reinterpret_cast<uint32_t*>(smem + L::kScrOff + wq * L::kScrWarpBytes) + lane;
 #pragma unroll
-            for (int pg = 0; pg < kBlockPages; ++pg) {
-              const uint32_t b = ((valid >> pg) & 1) ? lds8(raw + pg * P::kRawPageBytes +
-                                                            swz128(34 - P::kRawRow0 + (slot >> 3), (slot & 7) * 16 + blk))
-                                                     : 0u;
-              asm volatile("st.shared.u8 [%0], %1;" ::"r"(scr + pg * 32 + bsel * 16 + slot), "h"(static_cast<uint16_t>(b)));
+            for (int i = 0; i < kBlockPages / 2; ++i) {
+              const int pg = 2 * i + (lane >> 4);  // word lane + 32 i = (pg, bsel, fp)
+              const uint32_t b0 = lds8(raw + pg * P::kRawPageBytes + o0);
+              const uint32_t b1 = lds8(raw + pg * P::kRawPageBytes + o1);
+              const int s0 = 16 * pg + 2 * fp;
+              const bool pv = (valid >> pg) & 1;
+              const uint32_t m = (pv && s0 < keys_left ? 0x0000FFFFu : 0u) | (pv && s0 + 1 < keys_left ? 0xFFFF0000u : 0u);
+              fdst[32 * i] = e4m3x2_to_f16x2(b0 | (b1 << 8)) & m;
             }
           }
           __syncwarp();
@@ -510,22 +521,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 0; m < 4; ++m) cbase[m] = raw + swz128(code_row + 2 * m, code_col);
           uint32_t code[kBlockPages][8];
-          uint4 sc[kBlockPages];
+          uint4 sc[kBlockPages][2];
 #pragma unroll
           for (int pg = 0; pg < kBlockPages; ++pg) {
 #pragma unroll
             for (int pr = 0; pr < 8; ++pr)
               code[pg][pr] = lds8(cbase[pr & 3] + pg * P::kRawPageBytes + (pr >> 2) * 8 * 128);
-            sc[pg] = lds128(scr + pg * 32 + ((d >> 4) & 1) * 16);
+            sc[pg][0] = lds128(scr + (2 * pg + ((d >> 4) & 1)) * 32);
+            sc[pg][1] = lds128(scr + (2 * pg + ((d >> 4) & 1)) * 32 + 16);
           }
 #pragma unroll
           for (int pg = 0; pg < kBlockPages; ++pg) {
-            // a missing page: its scales in the scratch are zero
-            uint32_t sf[8];  // fp16x2 scales of slot pairs 0 .. 7
-            e4m3x4_to_f16x2x2(sc[pg].x, sf[0], sf[1]);
-            e4m3x4_to_f16x2x2(sc[pg].y, sf[2], sf[3]);
-            e4m3x4_to_f16x2x2(sc[pg].z, sf[4], sf[5]);
-            e4m3x4_to_f16x2x2(sc[pg].w, sf[6], sf[7]);
+            // fp16x2 scales of slot pairs 0 .. 7
+            const uint32_t sf[8] = {sc[pg][0].x, sc[pg][0].y, sc[pg][0].z, sc[pg][0].w,
+                                    sc[pg][1].x, sc[pg][1].y, sc[pg][1].z, sc[pg][1].w};
             uint32_t o[8];
 #pragma unroll
             for (int pr = 0; pr < 8; ++pr) o[pr] = hmul2(e2m1x2_to_f16x2(code[pg][pr]), sf[pr]);
@@ -733,16 +742,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // keys become -inf); the logit scale is positive, so the maximum of
         // the scaled logits is the scaled maximum
         const int key0 = (t.kb0 + j) * kBlockKeys;
-        float mraw = -INFINITY;
-        if (__all_sync(0xffffffffu, key0 + kBlockKeys <= lim)) {
+        if (!__all_sync(0xffffffffu, key0 + kBlockKeys <= lim)) {
 #pragma unroll
-          for (int k = 0; k < kBlockKeys; ++k) mraw = fmaxf(mraw, __uint_as_float(sr[k]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < kBlockKeys; ++k) {
+          for (int k = 0; k < kBlockKeys; ++k)
             if (key0 + k >= lim) sr[k] = __float_as_uint(-INFINITY);
-            mraw = fmaxf(mraw, __uint_as_float(sr[k]));
+        }
+        float mraw;
+        {
+          // two chains of three-input maxima over keys 0 .. 61, then 62, 63
+          float m0 = __uint_as_float(sr[0]), m1 = __uint_as_float(sr[1]);
+#pragma unroll
+          for (int k = 2; k + 3 < kBlockKeys; k += 4) {
+            m0 = fmax3(m0, __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+            m1 = fmax3(m1, __uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3]));
           }
+          mraw = fmax3(fmaxf(m0, m1), __uint_as_float(sr[kBlockKeys - 2]), __uint_as_float(sr[kBlockKeys - 1]));
         }
         const float mb = mraw * a.qk_scale_log2;
         // lazy rescale: move the exponent base only when the row max grows

@@ -45,6 +45,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Same with B MN-major (the N index contiguous in each 16-byte core-matrix
+// row).  A no-swizzle MN-major tile is 8 (K) x 16-byte (8 N) core matrices;
+// its descriptor's leading offset is the stride between core matrices
+// adjacent along K and its stride offset the one between core matrices
+// adjacent along N.
+__host__ __device__ constexpr uint32_t idesc_f16_bmn(int m, int n) { return idesc_f16(m, n) | (1u << 16); }
+
 // Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format 1), E4M3
 // scale factors (format bit 0), both K-major, dense K 64, fp32 D.
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int m, int n) {

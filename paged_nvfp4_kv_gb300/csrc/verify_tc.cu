@@ -26,7 +26,8 @@
 //                       row reference maximum that moves only when a row's
 //                       logits pass it by more than 2^8 (then the exact block
 //                       maxima are reduced and O^T and the row sums rescaled),
-//                       P^T (fp16) to shared memory, per-thread row sums
+//                       P^T (fp16, rows contiguous) to shared memory, per-
+//                       thread row sums
 //   K warps 4-7         K codes x block scales -> fp16 K rows in TMEM
 //   V warps 8-11        V codes x block scales -> fp16 V^T rows in TMEM (the
 //                       pool stores V slot-pair interleaved, so one code byte
@@ -69,18 +70,19 @@ constexpr float kMoveThreshold = 8.f;       // log2 units
 constexpr int kRawOff = 0;
 constexpr int kQOff = kRawOff + kRawStages * kRawStage;  // Q^T: fp16 [32 rows][256 dims], core matrices
 constexpr int kQBytes = kRowsN * 256 * 2;
-// P^T: fp16 [32 rows][128 keys], 8x8 core matrices with padded strides:
-// 144 bytes between neighbours along the keys and 2,336 between 8-row
-// groups, so that the 32 stores of a warp (16 key pairs, two row groups)
-// fall on distinct banks
-constexpr int kPLbo = 144, kPSbo = 16 * kPLbo + 32;
+// P^T: fp16 [128 keys][32 rows], the B of P.V stored MN-major (rows
+// contiguous): each 8-key group is four core matrices of 8 keys x 16 bytes
+// (rows 8c .. 8c + 7), 128 bytes apart, and the groups are 512 bytes apart.
+// A key's 32 probabilities are four 16-byte stores, and a warp's 32 keys
+// write each of them as 512 contiguous bytes.
+constexpr int kPRowChunk = 128, kPKeyGroup = 512;
 constexpr int kPOff = kQOff + kQBytes;
-constexpr int kPBytes = 4 * kPSbo;
-constexpr int kScrOff = kPOff + kPStages * kPBytes;      // per V warp: scales [page][4 blocks][16 slots]
-constexpr int kScrWarp = kUnitPages * 4 * 16;
+constexpr int kPBytes = (kUnitKeys / 8) * kPKeyGroup;
+// per V warp: fp16x2 block scales [page][4 blocks][8 slot pairs]
+constexpr int kScrOff = kPOff + kPStages * kPBytes;
+constexpr int kScrWarp = kUnitPages * 4 * 8 * 4;
 constexpr int kMrefOff = kScrOff + 4 * kScrWarp;         // float [32]: per-row reference maximum (log2)
-constexpr int kThrOff = kMrefOff + kRowsN * 4;           // float [32]: reference + threshold
-constexpr int kBaseOff = kThrOff + kRowsN * 4;           // float [32]: exponent base (reference, 0 if none)
+constexpr int kBaseOff = kMrefOff + kRowsN * 4;          // float [32]: exponent base (reference, 0 if none)
 constexpr int kLimOff = kBaseOff + kRowsN * 4;           // int [32]: keys row r may see
 constexpr int kAlphaOff = kLimOff + kRowsN * 4;          // float [32]: rescale factors
 constexpr int kXchgOff = kAlphaOff + kRowsN * 4;         // float [4 warps][32]: reductions
@@ -131,11 +133,6 @@ __device__ __forceinline__ uint64_t* vbar(uint8_t* smem, int i) {
 }
 
 __device__ __forceinline__ uint32_t par(int64_t g, int n) { return static_cast<uint32_t>((g / n) & 1); }
-
-// Byte offset of P^T element (row r, key k).
-__device__ __forceinline__ uint32_t p_off(int r, int k) {
-  return (r >> 3) * kPSbo + (k >> 3) * kPLbo + ((r & 7) << 4) + ((k & 7) << 1);
-}
 
 // The 32-bit TMEM word of a warp's lane quarter: lane 32 * quarter, column c.
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int quarter) {
@@ -311,14 +308,18 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (!ok) break;
         const bool live = ((raw_valid[rs] >> pg) & 1) && (pc.p0 + k) * kUnitKeys + key < pc.s.len;
         const uint32_t rawb = smem_addr(smem + kRawOff + rs * kRawStage);
-        uint4 sc = make_uint4(0, 0, 0, 0);
-        if (live) sc = lds128(rawb + kscale);
+        // every load first (the row's codes and its 16 block scales); a dead
+        // key's scales are zeroed, which zeroes its row whatever the codes
+        uint4 wv[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) wv[c] = lds128(rawb + kswz[c]);
+        uint4 sc = lds128(rawb + kscale);
+        if (!live) sc = make_uint4(0, 0, 0, 0);
         const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
         const uint32_t taddr = lane_base(tmem, q) + 128 * ks;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: dims 32c .. 32c + 31 (blocks 2c, 2c + 1)
-          uint4 w = make_uint4(0, 0, 0, 0);
-          if (live) w = lds128(rawb + kswz[c]);
+          const uint4 w = wv[c];
           const uint32_t sb = (scw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;  // the two blocks' scale bytes
           const uint32_t s2 = e4m3x2_to_f16x2(sb);
           const uint32_t s_lo = prmt(s2, s2, 0x1010u), s_hi = prmt(s2, s2, 0x3232u);
@@ -347,9 +348,12 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // -------------------------------------------------------- V widening
     // thread = dims d0 = 32 q + lane and d1 = 128 + d0 (TMEM lane 32 q + lane
     // of the V^T halves): per page and slot pair, one code byte -> the fp16
-    // pair of the two keys -> one TMEM column.  The warp first transposes
-    // its four 16-dim blocks' scale bytes of the unit's 8 pages into a
-    // scratch [page][block][slot]; slots past the sequence scale to 0.
+    // pair of the two keys -> one TMEM column.  The warp first converts the
+    // block scales of its four 16-dim blocks (2q, 2q + 1, 8 + 2q, 9 + 2q;
+    // each shared by 16 of its lanes) over the unit's 8 pages into a scratch
+    // of fp16 pairs [page][block][slot pair], slots past the sequence or in a
+    // page that was not loaded scaled to 0 -- which zeroes their values
+    // whatever the stale codes (E2M1 has no infinities).
     // Every raw row index below is a compile-time constant, so each byte
     // load is one instruction: the thread keeps its column's 8 swizzled
     // offsets (the 16-byte chunk of the column XOR the row's residue mod 8).
@@ -359,20 +363,15 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     uint32_t swz[8];
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8) swz[c8] = ((((col >> 4) ^ c8) & 7) << 4) | (col & 15);
-    // scratch fill: step it reads page it / 2, block index bi = 2 (it % 2) +
-    // lane / 16 (blocks 2q, 2q + 1, 8 + 2q, 9 + 2q), slot lane % 16: one
-    // page's two scale rows per instruction (at most a 2-way conflict)
-    const int sl = lane & 15;
-    const uint32_t srow = 34 + (sl >> 3);  // raw row of the slot's scales
-    uint32_t sfill[2];
-#pragma unroll
-    for (int par2 = 0; par2 < 2; ++par2) {
-      const int bi = (par2 << 1) | (lane >> 4);
-      const int blk = (bi >> 1) * 8 + 2 * q + (bi & 1);
-      sfill[par2] = swz128(srow, (sl & 7) * 16 + blk);
-    }
-    const uint32_t sdst = scr + sl + 16 * (lane >> 4);  // + (4 j + 2 (it % 2)) * 16
-    const uint32_t sread = scr + 16 * (lane >> 4);      // + (4 j + 2 hh) * 16
+    // scratch fill: lane -> block index fbi = lane / 8, slot pair fp = lane %
+    // 8; one word per page.  The scale of (slot s, block b) is byte 16 (s %
+    // 8) + b of raw row 34 + s / 8.
+    const int fbi = lane >> 3, fp = lane & 7;
+    const int fblk = (fbi >> 1) * 8 + 2 * q + (fbi & 1);
+    const uint32_t fo0 = swz128(34 + (fp >> 2), ((2 * fp) & 7) * 16 + fblk);
+    const uint32_t fo1 = swz128(34 + (fp >> 2), ((2 * fp + 1) & 7) * 16 + fblk);
+    uint32_t* fdst = reinterpret_cast<uint32_t*>(smem + kScrOff + q * kScrWarp) + lane;  // + 32 j
+    const uint32_t sread = scr + (lane >> 4) * 32;  // + (4 j + 2 hh) * 32: the 8 pairs of the lane's block
     int64_t g = 0;
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
@@ -383,13 +382,20 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         const uint32_t valid = raw_valid[rs];
         const uint32_t raw = smem_addr(smem + kRawOff + rs * kRawStage);
         const int keys_left = pc.s.len - (pc.p0 + k) * kUnitKeys;  // keys of the unit in the sequence
+        {
+          uint32_t b0[kUnitPages], b1[kUnitPages];
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          const int j = it >> 1;
-          const bool live = ((valid >> j) & 1) && 16 * j + sl < keys_left;
-          const uint32_t b = live ? lds8(raw + j * kRawPage + sfill[it & 1]) : 0u;
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(sdst + (4 * j + 2 * (it & 1)) * 16), "h"(static_cast<uint16_t>(b))
-                       : "memory");
+          for (int j = 0; j < kUnitPages; ++j) {
+            b0[j] = lds8(raw + j * kRawPage + fo0);
+            b1[j] = lds8(raw + j * kRawPage + fo1);
+          }
+#pragma unroll
+          for (int j = 0; j < kUnitPages; ++j) {
+            const int s0 = 16 * j + 2 * fp;  // the pair's first key in the unit
+            const bool pv = (valid >> j) & 1;
+            const uint32_t m = (pv && s0 < keys_left ? 0x0000FFFFu : 0u) | (pv && s0 + 1 < keys_left ? 0xFFFF0000u : 0u);
+            fdst[32 * j] = e4m3x2_to_f16x2(b0[j] | (b1[j] << 8)) & m;
+          }
         }
         __syncwarp();
         // the slot of this unit's V^T (allocation 2g + 1) is free once the
@@ -405,23 +411,26 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 1
           for (int j2 = 0; j2 < kUnitPages; j2 += 2) {  // two pages = 16 columns
-            uint32_t colw[16];
+            uint32_t code[16];
+            uint4 sc[4];
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
               const int j = j2 + jj;
-              const uint4 sc = lds128(sread + (4 * j + 2 * hh) * 16);
-              uint32_t sf[8];  // fp16x2 scales of slot pairs 0 .. 7 (zero past the sequence)
-              e4m3x4_to_f16x2x2(sc.x, sf[0], sf[1]);
-              e4m3x4_to_f16x2x2(sc.y, sf[2], sf[3]);
-              e4m3x4_to_f16x2x2(sc.z, sf[4], sf[5]);
-              e4m3x4_to_f16x2x2(sc.w, sf[6], sf[7]);
-              const bool pv = (valid >> j) & 1;
+              sc[2 * jj] = lds128(sread + (4 * j + 2 * hh) * 32);
+              sc[2 * jj + 1] = lds128(sread + (4 * j + 2 * hh) * 32 + 16);
 #pragma unroll
               for (int pr = 0; pr < 8; ++pr) {
                 const int row = 18 + 2 * pr + hh;  // compile-time
-                const uint32_t code = pv ? lds8(base[row & 7] + j * kRawPage + row * 128) : 0u;
-                colw[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code), sf[pr]);
+                code[8 * jj + pr] = lds8(base[row & 7] + j * kRawPage + row * 128);
               }
+            }
+            uint32_t colw[16];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const uint32_t sf[8] = {sc[2 * jj].x,     sc[2 * jj].y,     sc[2 * jj].z,     sc[2 * jj].w,
+                                      sc[2 * jj + 1].x, sc[2 * jj + 1].y, sc[2 * jj + 1].z, sc[2 * jj + 1].w};
+#pragma unroll
+              for (int pr = 0; pr < 8; ++pr) colw[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code[8 * jj + pr]), sf[pr]);
             }
             tmem_st16(lane_base(tmem, q) + 128 * vs + 64 * hh + 8 * j2, colw);
           }
@@ -441,7 +450,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // stalls the other's queue of products.
     if (lane == 0) {
       const bool qk = warp == kQkWarp;
-      const uint32_t idesc = idesc_f16(128, kRowsN);
+      const uint32_t idesc = idesc_f16(128, kRowsN), idesc_pv = idesc_f16_bmn(128, kRowsN);
       int64_t g = 0, npiece = 0;
       bool ok = true, issued = false;
       while (ok && walk.next(a, &pc)) {
@@ -469,12 +478,15 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t p_base = smem_addr(smem + kPOff + pb * kPBytes);
+            // the two halves' products interleaved: two independent
+            // accumulation chains for the tensor core
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of V^T, 2 key groups of P^T
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of V^T, 2 core matrices of P^T
+              for (int hh = 0; hh < 2; ++hh)
                 umma_f16_ta(tmem + kTO + 32 * hh, tmem + 128 * vs + 64 * hh + 8 * kk,
-                            smem_desc(p_base + 2 * kPLbo * kk, kPLbo, kPSbo), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+                            smem_desc(p_base + 2 * kPKeyGroup * kk, kPKeyGroup, kPRowChunk), idesc_pv,
+                            (k > 0 || kk > 0) ? 1u : 0u);
             umma_commit(bar(V_FREE_V + vs));
             umma_commit(bar(V_PV_DONE + pb));
           }
@@ -499,7 +511,6 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     const int q = warp;
     const int key = 32 * q + lane;
     float* mref = reinterpret_cast<float*>(smem + kMrefOff);
-    float* thr = reinterpret_cast<float*>(smem + kThrOff);
     float* basev = reinterpret_cast<float*>(smem + kBaseOff);
     int* lim = reinterpret_cast<int*>(smem + kLimOff);
     float* alpha = reinterpret_cast<float*>(smem + kAlphaOff);
@@ -548,7 +559,6 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       if (threadIdx.x < kRowsN) {
         const int r = threadIdx.x;
         mref[r] = -INFINITY;
-        thr[r] = -INFINITY;
         basev[r] = 0.f;
         lim[r] = r < rows ? (a.causal ? pc.s.len - pc.s.qlen + r / a.group + 1 : pc.s.len) : 0;
       }
@@ -567,25 +577,30 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         float x[kRowsN];
         bool viol = false;
         const int kg = (pc.p0 + k) * kUnitKeys + key;
-        // S^T column r of this key -> masked, scaled logits x (log2 units);
-        // the S slot is released at the end of the unit, so it can be read
-        // again after a reduction
+        // S^T column r of this key -> masked logits relative to the row's
+        // exponent base, x = s * scale - base (log2 units, one FFMA); the S
+        // slot is released at the end of the unit, so it can be read again
+        // after a reduction
         const bool unmasked = (pc.p0 + k + 1) * kUnitKeys <= vis_all;  // uniform over the CTA
         auto load_x = [&]() {
           uint32_t sr[kRowsN];
           tmem_ld32(lb + kTS + 32 * sb, sr);
           tmem_wait_ld();
-          if (unmasked) {
 #pragma unroll
-            for (int r = 0; r < kRowsN; ++r) x[r] = __uint_as_float(sr[r]) * a.qk_scale_log2;
-          } else {
+          for (int r4 = 0; r4 < kRowsN; r4 += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(basev + r4);
+            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[r4 + e] = fmaf(__uint_as_float(sr[r4 + e]), a.qk_scale_log2, -bv[e]);
+          }
+          if (!unmasked) {
 #pragma unroll
             for (int r4 = 0; r4 < kRowsN; r4 += 4) {
               const int4 l4 = *reinterpret_cast<const int4*>(lim + r4);
               const int lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                x[r4 + e] = kg < lv[e] ? __uint_as_float(sr[r4 + e]) * a.qk_scale_log2 : -INFINITY;
+                if (kg >= lv[e]) x[r4 + e] = -INFINITY;
             }
           }
         };
@@ -593,24 +608,30 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (ok) {
           tc_fence_after();
           load_x();
-          float over = -INFINITY;  // max over rows of (x - reference - threshold)
+          // a row's reference moves when its logits pass it by more than the
+          // threshold.  The first unit of a piece always reduces (it sets the
+          // references); after it every row either has a finite reference or
+          // sees no key of the piece at all (a row's visible keys are a
+          // prefix of the sequence, and the piece's first unit holds its
+          // first key), so the test is on x alone.
+          float o0 = x[0], o1 = x[1];
 #pragma unroll
-          for (int r4 = 0; r4 < kRowsN; r4 += 4) {
-            const float4 t4 = *reinterpret_cast<const float4*>(thr + r4);
-            over = fmaxf(over, fmaxf(fmaxf(x[r4] - t4.x, x[r4 + 1] - t4.y), fmaxf(x[r4 + 2] - t4.z, x[r4 + 3] - t4.w)));
+          for (int r = 2; r + 3 < kRowsN; r += 4) {  // rows 2 .. 29 in two chains
+            o0 = fmax3(o0, x[r], x[r + 1]);
+            o1 = fmax3(o1, x[r + 2], x[r + 3]);
           }
-          viol = over > 0.f;  // (x = -inf against thr = -inf gives NaN: no move)
+          viol = fmax3(fmaxf(o0, o1), x[kRowsN - 2], x[kRowsN - 1]) > kMoveThreshold;
         }
         meet((ok ? 1u : 0u) | (__any_sync(0xffffffffu, viol) ? 2u : 0u), &all_and, &any_or);
         if (!(all_and & 1u)) {
           ok = false;
           break;
         }
-        if (any_or & 2u) {
-          // some row's logits passed its reference: the unit's exact row
-          // maxima (warp transpose-reduction, then over the four warps) move
-          // the references that grew by more than the threshold
-          // (in place on x, which is read again from S^T afterwards)
+        if (k == 0 || (any_or & 2u)) {
+          // the unit's exact row maxima (warp transpose-reduction, then over
+          // the four warps, relative to the old bases) move the references
+          // that grew by more than the threshold; x is then recomputed
+          // against the new bases
 #pragma unroll
           for (int s = 16; s >= 1; s >>= 1) {
             const bool up = lane & s;
@@ -622,20 +643,19 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             }
           }
           xchg[q * 32 + lane] = x[0];  // the warp's maximum of row `lane`
-          load_x();
           named_bar_sync(1, 128);
           if (threadIdx.x < kRowsN) {
             const int r = threadIdx.x;
-            const float bm = fmaxf(fmaxf(xchg[r], xchg[32 + r]), fmaxf(xchg[64 + r], xchg[96 + r]));
+            const float bm = fmaxf(fmaxf(xchg[r], xchg[32 + r]), fmaxf(xchg[64 + r], xchg[96 + r])) + basev[r];
             const float m0 = mref[r];
             const bool move = bm > m0 + kMoveThreshold || (m0 == -INFINITY && bm > -INFINITY);
             const float mn = move ? bm : m0;
             alpha[r] = (move && m0 != -INFINITY) ? fast_exp2(m0 - mn) : 1.f;
             mref[r] = mn;
-            thr[r] = mn + kMoveThreshold;
             basev[r] = mn == -INFINITY ? 0.f : mn;
           }
           named_bar_sync(1, 128);
+          load_x();
 #pragma unroll
           for (int r = 0; r < kRowsN; ++r) l[r] *= alpha[r];
           if (k > 0) {
@@ -659,37 +679,24 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           }
         }
         if (!ok) continue;  // reported at the next meeting
-        // p = 2^(x - reference) (at most 2^threshold; 0 for masked keys)
+        // p = 2^x (at most 2^threshold; 0 for masked keys)
 #pragma unroll
-        for (int r4 = 0; r4 < kRowsN; r4 += 4) {
-          const float4 b4 = *reinterpret_cast<const float4*>(basev + r4);
-          const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[r4 + e] = fast_exp2(x[r4 + e] - bv[e]);
-            l[r4 + e] += x[r4 + e];
-          }
+        for (int r = 0; r < kRowsN; ++r) {
+          x[r] = fast_exp2(x[r]);
+          l[r] += x[r];
         }
         // P^T slot pb was last read by the P.V of unit g - kPStages
         if (g >= kPStages) ok = waitw(V_PV_DONE + pb, par(g - kPStages, kPStages));
         if (!ok) continue;
-        // P^T [32 rows][128 keys] fp16 (B of P.V): the lanes of a key pair
-        // swap halves so that the even key writes rows 0-15 and the odd key
-        // rows 16-31 as (even, odd) fp16 pairs; the padded core-matrix
-        // strides put a warp's 32 stores on distinct banks
+        // this key's 32 probabilities as fp16, four 16-byte pieces (rows
+        // 8c .. 8c + 7) of the MN-major P^T
         {
-          const int ke = key & ~1;
-          const bool odd = lane & 1;
-          // rows j (even key) or 16 + j (odd key): thread-constant base plus a
-          // compile-time offset per j
-          uint8_t* pt = smem + kPOff + pb * kPBytes + p_off(odd ? 16 : 0, ke);
+          uint8_t* pt = smem + kPOff + pb * kPBytes + (key >> 3) * kPKeyGroup + (key & 7) * 16;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float send = odd ? x[j] : x[16 + j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const float lo = odd ? recv : x[j], hi = odd ? x[16 + j] : recv;
-            *reinterpret_cast<uint32_t*>(pt + (j >> 3) * kPSbo + (j & 7) * 16) = f32x2_to_f16x2(lo, hi);
-          }
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(pt + c * kPRowChunk) =
+                make_uint4(f32x2_to_f16x2(x[8 * c], x[8 * c + 1]), f32x2_to_f16x2(x[8 * c + 2], x[8 * c + 3]),
+                           f32x2_to_f16x2(x[8 * c + 4], x[8 * c + 5]), f32x2_to_f16x2(x[8 * c + 6], x[8 * c + 7]));
           fence_proxy_async();
           tc_fence_before();
           __syncwarp();

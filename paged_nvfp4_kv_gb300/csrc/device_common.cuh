@@ -68,28 +68,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same with a bound on how long the thread may be suspended inside the test.
-__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait until the phase with the given parity has completed.  Returns false
 // (and the caller flags a timeout) if that takes longer than limit_ns.  Each
-// test may suspend the thread for at most a quarter of the bound (at most
-// 100 us), and the clock is read after every test, so a short bound is kept
-// to within about a quarter of itself.
+// test may suspend the thread for the hardware's own time limit (a few
+// microseconds); between tests the thread sleeps 20 ns and reads the clock, so
+// the bound is kept to within one test.  (Tests with an explicit suspend-time
+// hint measured a few percent slower in the tensor-core tiles.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint32_t hint = static_cast<uint32_t>(limit_ns / 4 < 100000ull ? limit_ns / 4 : 100000ull);
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_for(bar, parity, hint)) return true;
+    __nanosleep(20);
+    if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }

@@ -292,10 +292,23 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // stage; keys past the sequence or in a page that was not loaded are 0
     const int q = warp - kKWarp0;
     const int key = 32 * q + lane, pg = key >> 4, slot = key & 15;
-    uint32_t kswz[8];  // the slot's row with its 16-byte chunks swizzled
-#pragma unroll
-    for (int c = 0; c < 8; ++c) kswz[c] = pg * kRawPage + swz128(slot, 16 * c);
+    const uint32_t krow = pg * kRawPage + slot * 128;  // the slot's code row (chunks swizzled by slot % 8)
     const uint32_t kscale = pg * kRawPage + swz128(16 + (slot >> 3), (slot & 7) * 16);
+    // 16 code bytes (32 dims, blocks b and b + 1) and the two blocks' scale
+    // bytes -> 16 TMEM columns of fp16 pairs
+    auto widen = [](const uint4 w, uint32_t sb, uint32_t (&h)[16]) {
+      const uint32_t s2 = e4m3x2_to_f16x2(sb);
+      const uint32_t s_lo = prmt(s2, s2, 0x1010u), s_hi = prmt(s2, s2, 0x3232u);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t o4[4];
+        e2m1x8_unpack(ws[e], o4);
+        const uint32_t s = e < 2 ? s_lo : s_hi;
+#pragma unroll
+        for (int f = 0; f < 4; ++f) h[4 * e + f] = hmul2(o4[f], s);
+      }
+    };
     int64_t g = 0;
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
@@ -306,34 +319,23 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         // the slot's previous user is the V^T of unit g - 2 (allocation al - 3)
         ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) && (al < 3 || waitw(V_FREE_V + ks, use_parity(al - 3)));
         if (!ok) break;
+        // a dead key's scales are zeroed, which zeroes its row whatever the codes
         const bool live = ((raw_valid[rs] >> pg) & 1) && (pc.p0 + k) * kUnitKeys + key < pc.s.len;
+        const uint32_t smask = live ? 0xFFFFFFFFu : 0u;
         const uint32_t rawb = smem_addr(smem + kRawOff + rs * kRawStage);
-        // every load first (the row's codes and its 16 block scales); a dead
-        // key's scales are zeroed, which zeroes its row whatever the codes
-        uint4 wv[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) wv[c] = lds128(rawb + kswz[c]);
-        uint4 sc = lds128(rawb + kscale);
-        if (!live) sc = make_uint4(0, 0, 0, 0);
-        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
         const uint32_t taddr = lane_base(tmem, q) + 128 * ks;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: dims 32c .. 32c + 31 (blocks 2c, 2c + 1)
-          const uint4 w = wv[c];
-          const uint32_t sb = (scw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;  // the two blocks' scale bytes
-          const uint32_t s2 = e4m3x2_to_f16x2(sb);
-          const uint32_t s_lo = prmt(s2, s2, 0x1010u), s_hi = prmt(s2, s2, 0x3232u);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        // a runtime loop keeps the code small (the tile's roles share each
+        // SM sub-partition's instruction cache)
+#pragma unroll 1
+        for (int c2 = 0; c2 < 4; ++c2) {  // chunks 2 c2, 2 c2 + 1: dims 64 c2 .. + 63, blocks 4 c2 .. + 3
+          const uint4 w0 = lds128(rawb + krow + ((((2 * c2) ^ slot) & 7) << 4));
+          const uint4 w1 = lds128(rawb + krow + ((((2 * c2 + 1) ^ slot) & 7) << 4));
+          const uint32_t sw = lds32(rawb + kscale + 4 * c2) & smask;
           uint32_t h[16];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint32_t o4[4];
-            e2m1x8_unpack(ws[e], o4);
-            const uint32_t s = e < 2 ? s_lo : s_hi;
-#pragma unroll
-            for (int f = 0; f < 4; ++f) h[4 * e + f] = hmul2(o4[f], s);
-          }
-          tmem_st16(taddr + 16 * c, h);
+          widen(w0, sw & 0xFFFFu, h);
+          tmem_st16(taddr + 32 * c2, h);
+          widen(w1, sw >> 16, h);
+          tmem_st16(taddr + 32 * c2 + 16, h);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -605,29 +607,29 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           }
         };
         if (ok) ok = waitw(V_S_FULL + sb, par(g, 2));
-        if (ok) {
-          tc_fence_after();
-          load_x();
-          // a row's reference moves when its logits pass it by more than the
-          // threshold.  The first unit of a piece always reduces (it sets the
-          // references); after it every row either has a finite reference or
-          // sees no key of the piece at all (a row's visible keys are a
-          // prefix of the sequence, and the piece's first unit holds its
-          // first key), so the test is on x alone.
-          float o0 = x[0], o1 = x[1];
+        if (ok) tc_fence_after();
+        // one or two passes: x from S^T; after a reduction (which moves the
+        // bases) x is read again.  (One copy of the load keeps the code small.)
+        for (bool second = false;; second = true) {
+          if (ok) load_x();
+          if (second) break;
+          if (ok) {
+            // a row's reference moves when its logits pass it by more than
+            // the threshold.  The first unit of a piece always reduces (it
+            // sets the references); after it every row either has a finite
+            // reference or sees no key of the piece at all (a row's visible
+            // keys are a prefix of the sequence, and the piece's first unit
+            // holds its first key), so the test is on x alone.
+            float o0 = x[0], o1 = x[1];
 #pragma unroll
-          for (int r = 2; r + 3 < kRowsN; r += 4) {  // rows 2 .. 29 in two chains
-            o0 = fmax3(o0, x[r], x[r + 1]);
-            o1 = fmax3(o1, x[r + 2], x[r + 3]);
+            for (int r = 2; r + 3 < kRowsN; r += 4) {  // rows 2 .. 29 in two chains
+              o0 = fmax3(o0, x[r], x[r + 1]);
+              o1 = fmax3(o1, x[r + 2], x[r + 3]);
+            }
+            viol = fmax3(fmaxf(o0, o1), x[kRowsN - 2], x[kRowsN - 1]) > kMoveThreshold;
           }
-          viol = fmax3(fmaxf(o0, o1), x[kRowsN - 2], x[kRowsN - 1]) > kMoveThreshold;
-        }
-        meet((ok ? 1u : 0u) | (__any_sync(0xffffffffu, viol) ? 2u : 0u), &all_and, &any_or);
-        if (!(all_and & 1u)) {
-          ok = false;
-          break;
-        }
-        if (k == 0 || (any_or & 2u)) {
+          meet((ok ? 1u : 0u) | (__any_sync(0xffffffffu, viol) ? 2u : 0u), &all_and, &any_or);
+          if (!(all_and & 1u) || !(k == 0 || (any_or & 2u))) break;
           // the unit's exact row maxima (warp transpose-reduction, then over
           // the four warps, relative to the old bases) move the references
           // that grew by more than the threshold; x is then recomputed
@@ -655,7 +657,6 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             basev[r] = mn == -INFINITY ? 0.f : mn;
           }
           named_bar_sync(1, 128);
-          load_x();
 #pragma unroll
           for (int r = 0; r < kRowsN; ++r) l[r] *= alpha[r];
           if (k > 0) {
@@ -677,6 +678,10 @@ __global__ void __launch_bounds__(kThreadsV, 1)
               tc_fence_before();
             }
           }
+        }
+        if (!(all_and & 1u)) {
+          ok = false;
+          break;
         }
         if (!ok) continue;  // reported at the next meeting
         // p = 2^x (at most 2^threshold; 0 for masked keys)

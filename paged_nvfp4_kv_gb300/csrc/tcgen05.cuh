@@ -89,6 +89,15 @@ __device__ __forceinline__ void umma_fp4(uint32_t d_tmem, uint64_t a, uint64_t b
       : "memory");
 }
 
+// True in exactly one thread of the (converged) warp.  MMAs are issued by one
+// thread, but from warp-uniform control flow the operands stay in uniform
+// registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile("{ .reg .pred p; elect.sync _|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_addr(bar))

@@ -391,12 +391,18 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             b0[j] = lds8(raw + j * kRawPage + fo0);
             b1[j] = lds8(raw + j * kRawPage + fo1);
           }
+          if (valid == (1u << kUnitPages) - 1 && keys_left >= kUnitKeys) {  // every slot live (uniform)
 #pragma unroll
-          for (int j = 0; j < kUnitPages; ++j) {
-            const int s0 = 16 * j + 2 * fp;  // the pair's first key in the unit
-            const bool pv = (valid >> j) & 1;
-            const uint32_t m = (pv && s0 < keys_left ? 0x0000FFFFu : 0u) | (pv && s0 + 1 < keys_left ? 0xFFFF0000u : 0u);
-            fdst[32 * j] = e4m3x2_to_f16x2(b0[j] | (b1[j] << 8)) & m;
+            for (int j = 0; j < kUnitPages; ++j) fdst[32 * j] = e4m3x2_to_f16x2(prmt(b0[j], b1[j], 0x0040u));
+          } else {
+#pragma unroll
+            for (int j = 0; j < kUnitPages; ++j) {
+              const int s0 = 16 * j + 2 * fp;  // the pair's first key in the unit
+              const bool pv = (valid >> j) & 1;
+              const uint32_t m =
+                  (pv && s0 < keys_left ? 0x0000FFFFu : 0u) | (pv && s0 + 1 < keys_left ? 0xFFFF0000u : 0u);
+              fdst[32 * j] = e4m3x2_to_f16x2(prmt(b0[j], b1[j], 0x0040u)) & m;
+            }
           }
         }
         __syncwarp();
@@ -448,62 +454,72 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     }
   } else if (warp == kQkWarp || warp == kPvWarp) {
     // --------------------------------------------------------------- MMA
-    // QK and P.V from threads of different warps, so a wait of one never
-    // stalls the other's queue of products.
-    if (lane == 0) {
-      const bool qk = warp == kQkWarp;
-      const uint32_t idesc = idesc_f16(128, kRowsN), idesc_pv = idesc_f16_bmn(128, kRowsN);
-      int64_t g = 0, npiece = 0;
-      bool ok = true, issued = false;
-      while (ok && walk.next(a, &pc)) {
-        if (qk) ok = wait1(V_Q_FULL, static_cast<uint32_t>(npiece & 1));
-        for (int k = 0; ok && k < pc.n; ++k, ++g) {
-          if (qk) {
-            const int sb = static_cast<int>(g & 1);
-            const int64_t al = 2 * g;  // K of unit g
-            const int ks = slot_of(al);
-            ok = wait1(V_FULL_K + ks, use_parity(al)) && (g < 2 || wait1(V_S_FREE + sb, par(g - 2, 2)));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t q_base = smem_addr(smem + kQOff);
+    // QK and P.V from different warps, so a wait of one never stalls the
+    // other's queue of products.  The whole warp runs the loop and waits;
+    // one elected thread issues.  The shared-memory descriptors advance by
+    // their encoded address field (16-byte units) per product.
+    const bool qk = warp == kQkWarp;
+    const uint32_t idesc = idesc_f16(128, kRowsN), idesc_pv = idesc_f16_bmn(128, kRowsN);
+    const uint64_t qdesc = smem_desc(smem_addr(smem + kQOff), 128, 4096);
+    const uint64_t pdesc0 = smem_desc(smem_addr(smem + kPOff), kPKeyGroup, kPRowChunk);
+    int64_t g = 0, npiece = 0;
+    bool ok = true, issued = false;
+    while (ok && walk.next(a, &pc)) {
+      if (qk) ok = waitw(V_Q_FULL, static_cast<uint32_t>(npiece & 1));
+      for (int k = 0; ok && k < pc.n; ++k, ++g) {
+        if (qk) {
+          const int sb = static_cast<int>(g & 1);
+          const int64_t al = 2 * g;  // K of unit g
+          const int ks = slot_of(al);
+          ok = waitw(V_FULL_K + ks, use_parity(al)) && (g < 2 || waitw(V_S_FREE + sb, par(g - 2, 2)));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kTS + 32 * sb, a0 = tmem + 128 * ks;
+          if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk)  // 16 dims: 8 TMEM columns of K, 2 core matrices of Q^T
-              umma_f16_ta(tmem + kTS + 32 * sb, tmem + 128 * ks + 8 * kk,
-                          smem_desc(q_base + 256 * kk, 128, 4096), idesc, kk > 0);
+            for (int kk = 0; kk < 16; ++kk)  // 16 dims: 8 TMEM columns of K, 2 core matrices (256 B) of Q^T
+              umma_f16_ta(d, a0 + 8 * kk, qdesc + 16 * kk, idesc, kk > 0);
             umma_commit(bar(V_S_FULL + sb));
             umma_commit(bar(V_FREE_K + ks));
-          } else {
-            const int pb = static_cast<int>(g % kPStages);
-            const int64_t al = 2 * g + 1;  // V^T of unit g
-            const int vs = slot_of(al);
-            ok = wait1(V_FULL_V + vs, use_parity(al)) && wait1(V_P_FULL + pb, par(g, kPStages));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t p_base = smem_addr(smem + kPOff + pb * kPBytes);
+          }
+          __syncwarp();
+        } else {
+          const int pb = static_cast<int>(g % kPStages);
+          const int64_t al = 2 * g + 1;  // V^T of unit g
+          const int vs = slot_of(al);
+          ok = waitw(V_FULL_V + vs, use_parity(al)) && waitw(V_P_FULL + pb, par(g, kPStages));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(pb * (kPBytes >> 4));
+          const uint32_t a0 = tmem + 128 * vs;
+          const uint32_t acc = k > 0 ? 1u : 0u;
+          if (elect_one()) {
             // the two halves' products interleaved: two independent
             // accumulation chains for the tensor core
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of V^T, 2 key groups of P^T
+            for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of V^T, 2 key groups (1 KB) of P^T
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh)
-                umma_f16_ta(tmem + kTO + 32 * hh, tmem + 128 * vs + 64 * hh + 8 * kk,
-                            smem_desc(p_base + 2 * kPKeyGroup * kk, kPKeyGroup, kPRowChunk), idesc_pv,
-                            (k > 0 || kk > 0) ? 1u : 0u);
+                umma_f16_ta(tmem + kTO + 32 * hh, a0 + 64 * hh + 8 * kk, pdesc + 64 * kk, idesc_pv,
+                            kk > 0 ? 1u : acc);
             umma_commit(bar(V_FREE_V + vs));
             umma_commit(bar(V_PV_DONE + pb));
           }
-          issued = true;
+          __syncwarp();
         }
-        ++npiece;
+        issued = true;
       }
-      // every issued product completes before TMEM is released (fixed bound)
+      ++npiece;
+    }
+    // every issued product completes before TMEM is released (fixed bound)
+    if (elect_one()) {
       if (issued)
         umma_commit(bar(V_FINAL));
       else
         mbar_arrive(bar(V_FINAL));
-      mbar_wait(bar(V_FINAL), 0);
     }
     __syncwarp();
+    mbar_wait(bar(V_FINAL), 0);
   } else {
     // ----------------------------------------------------------- softmax
     // thread = key 32 q + lane of the unit (TMEM lane); columns = rows.  The

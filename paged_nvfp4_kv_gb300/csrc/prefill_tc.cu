@@ -552,79 +552,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp || warp == kQkWarp) {
     // --------------------------------------------------------------- MMA
-    // Two issuing threads in different warps: a shared-memory access of a
-    // thread (an mbarrier wait included) waits until the tensor core has
-    // taken the MMAs that thread issued before it, so the QK thread's waits
-    // never stall the P V stream and the other way round.
-    if (lane == 0) {
-      const bool qk_role = warp == kQkWarp;
-      const uint32_t idesc = qk_role ? (FP4Q ? idesc_mxf4nvf4(128, kBlockKeys) : idesc_f16(128, kBlockKeys))
-                                     : idesc_f16(128, 256);
-      int64_t gb = 0;  // first block of the current tile
-      int64_t tcount = 0;
-      bool ok = true, issued_any = false;
-      Tile t;
-      for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x, ++tcount) {
-        const int64_t g0 = gb;
-        if (qk_role) {
-          // Q of this tile is ready (fp16 in TMEM, or FP4 codes in shared
-          // memory with their scale factors in TMEM), written by the softmax warps
-          ok = wait(L::B_Q_FULL, static_cast<uint32_t>(tcount & 1));
-          for (int j = 0; ok && j < t.nblocks; ++j) {
-            const int64_t g = g0 + j;
-            const int ks = static_cast<int>(g % P::kKStages), ss = static_cast<int>(g % P::kSStages);
-            ok = wait(L::B_K_FULL + ks, ring_parity(g, P::kKStages)) &&
-                 (!FP4Q || wait(L::B_KC_FULL + ks, ring_parity(g, P::kKStages))) &&
-                 (g < P::kSStages || wait(L::B_S_FREE + ss, ring_parity(g - P::kSStages, P::kSStages)));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t k_base = smem_addr(smem + L::kKOff + ks * P::kKBytes);
+    // QK and P V from different warps: a shared-memory access of a thread
+    // (an mbarrier wait included) waits until the tensor core has taken the
+    // MMAs that thread issued before it, so the QK warp's waits never stall
+    // the P V stream and the other way round.  The whole warp runs the loop
+    // and waits, one elected thread issues (the operands stay in uniform
+    // registers), and the shared-memory descriptors advance by their encoded
+    // address field (16-byte units).
+    const bool qk_role = warp == kQkWarp;
+    const uint32_t idesc = qk_role ? (FP4Q ? idesc_mxf4nvf4(128, kBlockKeys) : idesc_f16(128, kBlockKeys))
+                                   : idesc_f16(128, 256);
+    const uint64_t kdesc0 =
+        FP4Q ? smem_desc_sw128(smem_addr(smem + L::kKOff)) : smem_desc(smem_addr(smem + L::kKOff), 128, 4096);
+    const uint64_t qdesc0 = FP4Q ? smem_desc_sw128(smem_addr(smem + L::kQOff)) : 0;
+    const uint64_t pdesc0 = smem_desc(smem_addr(smem + L::kPOff), 128, kBlockKeys * 16);
+    const uint64_t vdesc0 = smem_desc(smem_addr(smem + L::kVOff), 128, kBlockKeys * 16);
+    int64_t gb = 0;  // first block of the current tile
+    int64_t tcount = 0;
+    bool ok = true, issued_any = false;
+    Tile t;
+    for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x, ++tcount) {
+      const int64_t g0 = gb;
+      if (qk_role) {
+        // Q of this tile is ready (fp16 in TMEM, or FP4 codes in shared
+        // memory with their scale factors in TMEM), written by the softmax warps
+        ok = wait_warp(L::B_Q_FULL, static_cast<uint32_t>(tcount & 1));
+        for (int j = 0; ok && j < t.nblocks; ++j) {
+          const int64_t g = g0 + j;
+          const int ks = static_cast<int>(g % P::kKStages), ss = static_cast<int>(g % P::kSStages);
+          ok = wait_warp(L::B_K_FULL + ks, ring_parity(g, P::kKStages)) &&
+               (!FP4Q || wait_warp(L::B_KC_FULL + ks, ring_parity(g, P::kKStages))) &&
+               (g < P::kSStages || wait_warp(L::B_S_FREE + ss, ring_parity(g - P::kSStages, P::kSStages)));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(ks * (P::kKBytes >> 4));
+          const uint32_t d = tmem + L::kTmemS + ss * kBlockKeys;
+          if (elect_one()) {
             if constexpr (FP4Q) {
-              const uint32_t q_base = smem_addr(smem + L::kQOff);
 #pragma unroll
               for (int c = 0; c < 4; ++c)  // 64 FP4 elements = 32 bytes of every row per K-chunk
-                umma_fp4(tmem + L::kTmemS + ss * kBlockKeys, smem_desc_sw128(q_base + 32 * c),
-                         smem_desc_sw128(k_base + 32 * c), idesc, tmem + P::kTmemSfa + 4 * c,
+                umma_fp4(d, qdesc0 + 2 * c, kdesc + 2 * c, idesc, tmem + P::kTmemSfa + 4 * c,
                          tmem + P::kTmemSfb + ks * 16 + 4 * c, c > 0);
             } else {
 #pragma unroll
-              for (int kk = 0; kk < 16; ++kk)  // 16 dims = 8 TMEM columns of Q per k-step
-                umma_f16_ta(tmem + L::kTmemS + ss * kBlockKeys, tmem + P::kTmemQ + kk * 8,
-                            smem_desc(k_base + kk * 256, 128, 4096), idesc, kk > 0);
+              for (int kk = 0; kk < 16; ++kk)  // 16 dims = 8 TMEM columns of Q, 2 core matrices (256 B) of K
+                umma_f16_ta(d, tmem + P::kTmemQ + kk * 8, kdesc + 16 * kk, idesc, kk > 0);
             }
             umma_commit(bar(L::B_S_FULL + ss));
             umma_commit(bar(L::B_K_FREE + ks));
-            issued_any = true;
           }
-        } else {
-          for (int j = 0; ok && j < t.nblocks; ++j) {
-            const int64_t g = g0 + j;
-            const int ps = static_cast<int>(g % P::kPStages), vs = static_cast<int>(g % P::kVStages);
-            ok = wait(L::B_P_FULL + ps, ring_parity(g, P::kPStages)) &&
-                 wait(L::B_V_FULL + vs, ring_parity(g, P::kVStages));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t p_base = smem_addr(smem + L::kPOff + ps * L::kPBytes);
-            const uint32_t v_base = smem_addr(smem + L::kVOff + vs * L::kVBytes);
+          __syncwarp();
+          issued_any = true;
+        }
+      } else {
+        for (int j = 0; ok && j < t.nblocks; ++j) {
+          const int64_t g = g0 + j;
+          const int ps = static_cast<int>(g % P::kPStages), vs = static_cast<int>(g % P::kVStages);
+          ok = wait_warp(L::B_P_FULL + ps, ring_parity(g, P::kPStages)) &&
+               wait_warp(L::B_V_FULL + vs, ring_parity(g, P::kVStages));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(ps * (L::kPBytes >> 4));
+          const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(vs * (L::kVBytes >> 4));
+          const uint32_t acc = j > 0 ? 1u : 0u;
+          if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-              umma_f16(tmem + L::kTmemO, smem_desc(p_base + kk * 256, 128, kBlockKeys * 16),
-                       smem_desc(v_base + kk * 256, 128, kBlockKeys * 16), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBlockKeys / 16; ++kk)  // 16 keys = 2 core matrices (256 B) of P and of V^T
+              umma_f16(tmem + L::kTmemO, pdesc + 16 * kk, vdesc + 16 * kk, idesc, kk > 0 ? 1u : acc);
             umma_commit(bar(L::B_V_FREE + vs));
             umma_commit(bar(L::B_PV_DONE + ps));
-            issued_any = true;
           }
+          __syncwarp();
+          issued_any = true;
         }
-        gb = g0 + t.nblocks;
       }
-      // every issued MMA completes before TMEM is released (fixed bound)
+      gb = g0 + t.nblocks;
+    }
+    // every issued MMA completes before TMEM is released (fixed bound)
+    if (elect_one()) {
       if (issued_any)
         umma_commit(bar(L::B_FINAL));
       else
         mbar_arrive(bar(L::B_FINAL));
-      mbar_wait(bar(L::B_FINAL), 0);
     }
     __syncwarp();
+    mbar_wait(bar(L::B_FINAL), 0);
   } else {
     // ----------------------------------------------------------- softmax
     const int r = threadIdx.x;  // row = TMEM lane (warps 0-3)

@@ -304,6 +304,14 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t byte) {
 }
 
 
+// Four E2M1 codes (the low 16 bits of w, element 2k in the low nibble of byte
+// k) -> two f16x2 values, o[k] = (element 2k, element 2k+1) of byte k.  Exact.
+__device__ __forceinline__ void e2m1x4_unpack(uint32_t w, uint32_t (&o)[2]) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %2;"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1; }"
+      : "=r"(o[0]), "=r"(o[1]) : "r"(w));
+}
+
 // Eight E2M1 codes (one 32-bit word, element 2k in the low nibble of byte k)
 // -> four f16x2 values, o[k] = (element 2k, element 2k+1) of byte k.  Exact.
 __device__ __forceinline__ void e2m1x8_unpack(uint32_t w, uint32_t (&o)[4]) {

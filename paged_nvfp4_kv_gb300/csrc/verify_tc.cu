@@ -325,17 +325,35 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         const uint32_t rawb = smem_addr(smem + kRawOff + rs * kRawStage);
         const uint32_t taddr = lane_base(tmem, q) + 128 * ks;
         // a runtime loop keeps the code small (the tile's roles share each
-        // SM sub-partition's instruction cache)
-#pragma unroll 1
-        for (int c2 = 0; c2 < 4; ++c2) {  // chunks 2 c2, 2 c2 + 1: dims 64 c2 .. + 63, blocks 4 c2 .. + 3
-          const uint4 w0 = lds128(rawb + krow + ((((2 * c2) ^ slot) & 7) << 4));
-          const uint4 w1 = lds128(rawb + krow + ((((2 * c2 + 1) ^ slot) & 7) << 4));
-          const uint32_t sw = lds32(rawb + kscale + 4 * c2) & smask;
+        // SM sub-partition's instruction cache); two operand sets in turn, so
+        // that each step's loads are issued before the previous step is
+        // converted (the last look-ahead wraps to step 0: in bounds, unused)
+        const uint32_t kr = rawb + krow;
+        struct KOps {
+          uint4 w0, w1;
+          uint32_t sw;
+        };
+        auto kload = [&](int c2, KOps& o) {  // chunks 2 c2, 2 c2 + 1: dims 64 c2 .. + 63, blocks 4 c2 .. + 3
+          o.w0 = lds128(kr + ((((2 * c2) ^ slot) & 7) << 4));
+          o.w1 = lds128(kr + ((((2 * c2 + 1) ^ slot) & 7) << 4));
+          o.sw = lds32(rawb + kscale + 4 * c2);
+        };
+        auto kwiden = [&](int c2, const KOps& o) {
+          const uint32_t sw = o.sw & smask;
           uint32_t h[16];
-          widen(w0, sw & 0xFFFFu, h);
+          widen(o.w0, sw & 0xFFFFu, h);
           tmem_st16(taddr + 32 * c2, h);
-          widen(w1, sw >> 16, h);
+          widen(o.w1, sw >> 16, h);
           tmem_st16(taddr + 32 * c2 + 16, h);
+        };
+        KOps ka, kb;
+        kload(0, ka);
+#pragma unroll 1
+        for (int c2 = 0; c2 < 4; c2 += 2) {
+          kload(c2 + 1, kb);
+          kwiden(c2, ka);
+          kload((c2 + 2) & 3, ka);
+          kwiden(c2 + 1, kb);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -348,32 +366,37 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     }
   } else if (warp >= kVWarp0 && warp < kVWarp0 + 4) {
     // -------------------------------------------------------- V widening
-    // thread = dims d0 = 32 q + lane and d1 = 128 + d0 (TMEM lane 32 q + lane
-    // of the V^T halves): per page and slot pair, one code byte -> the fp16
-    // pair of the two keys -> one TMEM column.  The warp first converts the
-    // block scales of its four 16-dim blocks (2q, 2q + 1, 8 + 2q, 9 + 2q;
-    // each shared by 16 of its lanes) over the unit's 8 pages into a scratch
-    // of fp16 pairs [page][block][slot pair], slots past the sequence or in a
-    // page that was not loaded scaled to 0 -- which zeroes their values
-    // whatever the stale codes (E2M1 has no infinities).
-    // Every raw row index below is a compile-time constant, so each byte
-    // load is one instruction: the thread keeps its column's 8 swizzled
-    // offsets (the 16-byte chunk of the column XOR the row's residue mod 8).
+    // thread = TMEM lane L = 32 q + lane of the V^T halves, dims 2L (half 0)
+    // and 2L + 1 (half 1): the V^T accumulator's lane L, half h is dim
+    // 2L + h (the product does not care how dims map to lanes, only the
+    // epilogue does).  Dims 2L, 2L + 1 are adjacent bytes of one slot-pair
+    // row (rows 18 .. 25 + 2 pr hold dims 0 .. 127 of pair pr, the next rows
+    // dims 128 .. 255), so one 16-bit load gives both, and both lie in block
+    // L / 8, whose scales the 8 lanes of that block share.  The warp first
+    // converts the block scales of its four blocks (4q .. 4q + 3) over the
+    // unit's 8 pages into a scratch of fp16 pairs [page][block][slot pair];
+    // slots past the sequence or in a page that was not loaded scale to 0,
+    // which zeroes their values whatever the stale codes (E2M1 has no
+    // infinities).
     const int q = warp - kVWarp0;
     const uint32_t scr = smem_addr(smem + kScrOff + q * kScrWarp);
-    const uint32_t col = 32 * q + lane;  // byte of a 128-byte half-row: d & 127
-    uint32_t swz[8];
+    const int L = 32 * q + lane;
+    const uint32_t hrow = 18 + (L >> 6);   // slot-pair row of pair 0 for this lane's dims
+    const uint32_t col = (2 * L) & 127;    // their byte in that row
+    // swizzled offsets of pairs 0 .. 3 (pairs 4 .. 7 are 8 rows = 1,024 bytes
+    // further, with the same residues mod 8)
+    uint32_t cofs[4];
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) swz[c8] = ((((col >> 4) ^ c8) & 7) << 4) | (col & 15);
-    // scratch fill: lane -> block index fbi = lane / 8, slot pair fp = lane %
-    // 8; one word per page.  The scale of (slot s, block b) is byte 16 (s %
-    // 8) + b of raw row 34 + s / 8.
-    const int fbi = lane >> 3, fp = lane & 7;
-    const int fblk = (fbi >> 1) * 8 + 2 * q + (fbi & 1);
+    for (int m = 0; m < 4; ++m) cofs[m] = swz128(hrow + 2 * m, col);
+    // scratch fill: lane -> block 4q + lane / 8, slot pair fp = lane % 8;
+    // one word per page.  The scale of (slot s, block b) is byte 16 (s % 8)
+    // + b of raw row 34 + s / 8.
+    const int fp = lane & 7;
+    const int fblk = 4 * q + (lane >> 3);
     const uint32_t fo0 = swz128(34 + (fp >> 2), ((2 * fp) & 7) * 16 + fblk);
     const uint32_t fo1 = swz128(34 + (fp >> 2), ((2 * fp + 1) & 7) * 16 + fblk);
     uint32_t* fdst = reinterpret_cast<uint32_t*>(smem + kScrOff + q * kScrWarp) + lane;  // + 32 j
-    const uint32_t sread = scr + (lane >> 4) * 32;  // + (4 j + 2 hh) * 32: the 8 pairs of the lane's block
+    const uint32_t sread = scr + (lane >> 3) * 32;  // + 128 j: the 8 pairs of the lane's block
     int64_t g = 0;
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
@@ -412,36 +435,43 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         const int vs = slot_of(al);
         if (al >= 3) ok = waitw(V_FREE_K + vs, use_parity(al - 3));
         if (!ok) break;
-        uint32_t base[8];  // raw + this thread's swizzled column for each row residue
+        const uint32_t taddr = lane_base(tmem, q) + 128 * vs;
+        // operands of page j: its 8 pair scales and 8 code pairs
+        struct VOps {
+          uint4 s0, s1;
+          uint32_t code[8];
+        };
+        auto vload = [&](int j, VOps& o) {
+          const uint32_t pg = raw + j * kRawPage;
+          o.s0 = lds128(sread + j * 128);
+          o.s1 = lds128(sread + j * 128 + 16);
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) base[c8] = raw + swz[c8];
+          for (int pr = 0; pr < 8; ++pr) o.code[pr] = lds16(pg + cofs[pr & 3] + (pr >> 2) * 1024);
+        };
+        auto vwiden = [&](int j, const VOps& o) {  // page j = 8 columns of each half
+          const uint32_t sf[8] = {o.s0.x, o.s0.y, o.s0.z, o.s0.w, o.s1.x, o.s1.y, o.s1.z, o.s1.w};
+          uint32_t h0[8], h1[8];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll 1
-          for (int j2 = 0; j2 < kUnitPages; j2 += 2) {  // two pages = 16 columns
-            uint32_t code[16];
-            uint4 sc[4];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              const int j = j2 + jj;
-              sc[2 * jj] = lds128(sread + (4 * j + 2 * hh) * 32);
-              sc[2 * jj + 1] = lds128(sread + (4 * j + 2 * hh) * 32 + 16);
-#pragma unroll
-              for (int pr = 0; pr < 8; ++pr) {
-                const int row = 18 + 2 * pr + hh;  // compile-time
-                code[8 * jj + pr] = lds8(base[row & 7] + j * kRawPage + row * 128);
-              }
-            }
-            uint32_t colw[16];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              const uint32_t sf[8] = {sc[2 * jj].x,     sc[2 * jj].y,     sc[2 * jj].z,     sc[2 * jj].w,
-                                      sc[2 * jj + 1].x, sc[2 * jj + 1].y, sc[2 * jj + 1].z, sc[2 * jj + 1].w};
-#pragma unroll
-              for (int pr = 0; pr < 8; ++pr) colw[8 * jj + pr] = hmul2(e2m1x2_to_f16x2(code[8 * jj + pr]), sf[pr]);
-            }
-            tmem_st16(lane_base(tmem, q) + 128 * vs + 64 * hh + 8 * j2, colw);
+          for (int pr = 0; pr < 8; ++pr) {
+            uint32_t o2[2];
+            e2m1x4_unpack(o.code[pr], o2);  // byte 0: dim 2L, byte 1: dim 2L + 1
+            h0[pr] = hmul2(o2[0], sf[pr]);
+            h1[pr] = hmul2(o2[1], sf[pr]);
           }
+          tmem_st8(taddr + 8 * j, h0);
+          tmem_st8(taddr + 64 + 8 * j, h1);
+        };
+        // two operand sets in turn: each page's loads are issued before the
+        // previous page is converted (the last look-ahead wraps to page 0:
+        // in bounds, unused)
+        VOps va, vb;
+        vload(0, va);
+#pragma unroll 1
+        for (int j = 0; j < kUnitPages; j += 2) {
+          vload(j + 1, vb);
+          vwiden(j, va);
+          vload((j + 2) & (kUnitPages - 1), va);
+          vwiden(j + 1, vb);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -753,19 +783,20 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       const int64_t slot = pc.b * static_cast<int64_t>(a.hkv) + pc.h + blockIdx.x;
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 2 * kRowsN; c += 16) {  // both halves, 16 rows at a time
-        uint32_t o[16];
-        tmem_ld16(lb + kTO + c, o);
+      for (int c = 0; c < kRowsN; c += 8) {  // 8 rows at a time: O^T lane `key`, half h = dim 2 key + h
+        uint32_t o0[8], o1[8];
+        tmem_ld8(lb + kTO + c, o0);
+        tmem_ld8(lb + kTO + 32 + c, o1);
         tmem_wait_ld();
-        const int d = 128 * (c >> 5) + key;  // this lane's dim
         if (slot < a.part_slots) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int r = (c + e) & 31;
+          for (int e = 0; e < 8; ++e) {
+            const int r = c + e;
             if (r < rows) {
               const float L = alpha[r];
-              a.o_part[(slot * a.rows_per_slot + r) * 256 + d] =
-                  L > 0.f ? __uint_as_float(o[e]) * (a.out_scale / L) : 0.f;
+              const float f = L > 0.f ? a.out_scale / L : 0.f;
+              *reinterpret_cast<float2*>(a.o_part + (slot * a.rows_per_slot + r) * 256 + 2 * key) =
+                  make_float2(__uint_as_float(o0[e]) * f, __uint_as_float(o1[e]) * f);
             }
           }
         }

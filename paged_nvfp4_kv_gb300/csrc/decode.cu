@@ -783,11 +783,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
       const int32_t* row = a.page_table + static_cast<int64_t>(pc.b) * a.pt_stride + pc.p0;
+      // the next group's page ids are read while this group issues
+      int32_t next_page = lane < pc.n ? __ldg(row + lane) : 0;
       for (int j0 = 0; j0 < pc.n && ok; j0 += 32) {
         // lane j handles unit j0 + j: its own page id, stage and barrier;
         // lanes issue in groups of kIssueLanes so the ring refills steadily
         const bool mine = j0 + lane < pc.n;
-        const int32_t page = mine ? __ldg(row + j0 + lane) : 0;
+        const int32_t page = next_page;
+        next_page = j0 + 32 + lane < pc.n ? __ldg(row + j0 + 32 + lane) : 0;
         bool lane_ok = true;
 #pragma unroll 1
         for (int g = 0; g < 32 / P::kIssue; ++g) {

@@ -349,7 +349,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t ti = blockIdx.x; ok && find_tile(a, ti, &t); ti += gridDim.x) {
       const int32_t* row = a.page_table + static_cast<int64_t>(t.b) * a.pt_stride;
       const int pages = (t.len + 15) >> 4;
+      // page ids eight blocks at a time (lane l: block j0 + l / 4, page
+      // l % 4), loaded a group ahead, so that no table read sits between a
+      // free slot and its loads
+      auto load_ids = [&](int j0) -> int32_t {
+        const int jb = j0 + (lane >> 2);
+        const int pi = kBlockPages * (t.kb0 + jb) + (lane & 3);
+        return (jb < t.nblocks && pi < pages) ? __ldg(row + pi) : -1;
+      };
+      static_assert(kBlockPages == 4, "the id groups assume four pages per block");
+      int32_t ids = load_ids(0), ids_next = load_ids(8);
       for (int j = 0; j < t.nblocks && ok; ++j, ++gb) {
+        if (j > 0 && (j & 7) == 0) {
+          ids = ids_next;
+          ids_next = load_ids(j + 8);
+        }
+        int32_t page = __shfl_sync(0xffffffffu, ids, ((j & 7) << 2) | (lane & 3));
         const int rs = static_cast<int>(gb % P::kRawStages);
         const int ks = static_cast<int>(gb % P::kKStages);
         if (lane == 0) {
@@ -360,16 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         // lanes 0 .. kBlockPages - 1: the block's pages
-        int32_t page = -1;
-        if (lane < kBlockPages) {
-          const int pi = kBlockPages * (t.kb0 + j) + lane;
-          if (pi < pages) {
-            page = __ldg(row + pi);
-            if (page < 0 || page >= a.num_pages) {
-              flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
-              page = -1;
-            }
+        if (lane < kBlockPages && kBlockPages * (t.kb0 + j) + lane < pages) {
+          if (page < 0 || page >= a.num_pages) {
+            flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
+            page = -1;
           }
+        } else {
+          page = -1;
         }
         const unsigned load = __ballot_sync(0xffffffffu, lane < kBlockPages && page >= 0);
         if (lane == 0) {

@@ -63,6 +63,11 @@ constexpr int kRawPage = 5120;              // 4,608-byte record in a 1,024-alig
 constexpr int kRawStage = kUnitPages * kRawPage;
 constexpr uint32_t kRecBytesV = 4608;
 constexpr int kPStages = 2;
+// TMEM slots (128 columns each) of widened K and of widened V^T.  K's slot is
+// freed by the QK that read it, so one slot keeps the K widening one QK
+// behind; V^T's are freed by the P.V, which waits for the softmax, so V^T
+// gets two.
+constexpr int kKSlots = 1, kVSlots = 2;
 constexpr float kLn2V = 0.6931471805599453f;
 constexpr float kMoveThreshold = 8.f;       // log2 units
 
@@ -86,19 +91,18 @@ constexpr int kBaseOff = kMrefOff + kRowsN * 4;          // float [32]: exponent
 constexpr int kLimOff = kBaseOff + kRowsN * 4;           // int [32]: keys row r may see
 constexpr int kAlphaOff = kLimOff + kRowsN * 4;          // float [32]: rescale factors
 constexpr int kXchgOff = kAlphaOff + kRowsN * 4;         // float [4 warps][32]: reductions
-constexpr int kFlagOff = kXchgOff + 4 * kRowsN * 4;      // uint [4]: softmax warps' flags
-constexpr int kBarOffV = (kFlagOff + 16 + 7) & ~7;
+constexpr int kFlagOff = kXchgOff + 4 * kRowsN * 4;      // uint [2][4]: softmax warps' flags, two rounds
+constexpr int kBarOffV = (kFlagOff + 32 + 7) & ~7;
 enum {
   V_RAW_FULL = 0,
   V_RAW_EMPTY = V_RAW_FULL + kRawStages,
-  // per slot and per role, so that each barrier has one producer and its
-  // phases come in order: K or V^T widened into the slot; the QK or P.V
-  // that read it completed
+  // K and V^T slots: widened into the slot; the QK or P.V that read it
+  // completed
   V_FULL_K = V_RAW_EMPTY + kRawStages,
-  V_FULL_V = V_FULL_K + 3,
-  V_FREE_K = V_FULL_V + 3,
-  V_FREE_V = V_FREE_K + 3,
-  V_S_FULL = V_FREE_V + 3,
+  V_FULL_V = V_FULL_K + kKSlots,
+  V_FREE_K = V_FULL_V + kVSlots,
+  V_FREE_V = V_FREE_K + kKSlots,
+  V_S_FULL = V_FREE_V + kVSlots,
   V_S_FREE = V_S_FULL + 2,
   V_P_FULL = V_S_FREE + 2,
   V_PV_DONE = V_P_FULL + kPStages,
@@ -111,22 +115,11 @@ constexpr int kSmemV = kMiscOffV + 64 + 1024;
 static_assert(kSmemV <= 232448, "verify tile shared memory plan too large");
 static_assert(kQOff % 1024 == 0, "raw ring slots need 1,024-byte alignment");
 
-// TMEM columns: three 128-column slots that K and V^T take in turn (unit g's
-// K is allocation 2g, its V^T allocation 2g + 1, allocation a in slot a % 3;
-// V^T's halves at +0 and +64), then S^T (two stages of 32) and O^T (halves of
-// 32).  A slot is freed by the product that read it, so the V^T of unit g + 1
-// waits only for the QK of unit g, and the K of unit g + 1 for the P.V of
-// unit g - 1.
+// TMEM columns: the K slots, the V^T slots (halves at +0 and +64), then S^T
+// (two stages of 32) and O^T (halves of 32).
 constexpr uint32_t kTmemColsV = 512;
-constexpr uint32_t kTS = 384, kTO = 448;
-
-// Slot of allocation a, and the parity of its phase on its role's barriers of
-// that slot: a slot's uses by one role are 6 allocations apart (K uses are
-// even, V^T uses odd, both in a fixed residue mod 3), so allocation a is that
-// role's use number a / 6 of the slot.  The previous user of a's slot is
-// allocation a - 3, of the other role.
-__device__ __forceinline__ int slot_of(int64_t a) { return static_cast<int>(a % 3); }
-__device__ __forceinline__ uint32_t use_parity(int64_t a) { return static_cast<uint32_t>((a / 6) & 1); }
+constexpr uint32_t kTK = 0, kTV = 128 * kKSlots, kTS = 384, kTO = 448;
+static_assert(kTV + 128 * kVSlots <= kTS, "TMEM plan: K and V^T slots overlap S^T");
 
 __device__ __forceinline__ uint64_t* vbar(uint8_t* smem, int i) {
   return reinterpret_cast<uint64_t*>(smem + kBarOffV) + i;
@@ -156,10 +149,12 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       mbar_init(bar(V_RAW_EMPTY + i), 8);  // the K and the V warps
       raw_armed[i] = -1;
     }
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < kKSlots; ++i) {
       mbar_init(bar(V_FULL_K + i), 4);
-      mbar_init(bar(V_FULL_V + i), 4);
       mbar_init(bar(V_FREE_K + i), 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(bar(V_FULL_V + i), 4);
       mbar_init(bar(V_FREE_V + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -250,21 +245,32 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     bool ok = true;
     while (ok && walk.next(a, &pc)) {
       const int32_t* row = a.page_table + static_cast<int64_t>(pc.b) * a.pt_stride;
+      // page ids four units at a time (lane l: unit k0 + l / 8, page l % 8),
+      // loaded a group ahead, so that no table read sits between a free
+      // slot and its loads
+      auto load_ids = [&](int k0) -> int32_t {
+        const int u = k0 + (lane >> 3);
+        const int pi = (pc.p0 + u) * kUnitPages + (lane & 7);
+        return (u < pc.n && pi < pc.s.pages) ? __ldg(row + pi) : -1;
+      };
+      int32_t ids = load_ids(0), ids_next = load_ids(4);
       for (int k = 0; k < pc.n && ok; ++k, ++g) {
+        if (k > 0 && (k & 3) == 0) {
+          ids = ids_next;
+          ids_next = load_ids(k + 4);
+        }
+        int32_t page = __shfl_sync(0xffffffffu, ids, ((k & 3) << 3) | (lane & 7));
         const int rs = static_cast<int>(g % kRawStages);
         if (lane == 0) ok = wait1(V_RAW_EMPTY + rs, par(g, kRawStages) ^ 1u);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        int32_t page = -1;
-        if (lane < kUnitPages) {
-          const int pi = (pc.p0 + k) * kUnitPages + lane;
-          if (pi < pc.s.pages) {
-            page = __ldg(row + pi);
-            if (page < 0 || page >= a.num_pages) {
-              flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
-              page = -1;
-            }
+        if (lane < kUnitPages && (pc.p0 + k) * kUnitPages + lane < pc.s.pages) {
+          if (page < 0 || page >= a.num_pages) {
+            flag_error(a.dev_err, PNKV_DEV_ERR_PAGE_ID);
+            page = -1;
           }
+        } else {
+          page = -1;
         }
         const unsigned load = __ballot_sync(0xffffffffu, lane < kUnitPages && page >= 0);
         if (lane == 0) {
@@ -314,16 +320,16 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     while (ok && walk.next(a, &pc)) {
       for (int k = 0; k < pc.n && ok; ++k, ++g) {
         const int rs = static_cast<int>(g % kRawStages);
-        const int64_t al = 2 * g;  // this unit's K allocation
-        const int ks = slot_of(al);
-        // the slot's previous user is the V^T of unit g - 2 (allocation al - 3)
-        ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) && (al < 3 || waitw(V_FREE_V + ks, use_parity(al - 3)));
+        const int ks = static_cast<int>(g % kKSlots);
+        // the slot's previous user is the QK of unit g - kKSlots
+        ok = waitw(V_RAW_FULL + rs, par(g, kRawStages)) &&
+             (g < kKSlots || waitw(V_FREE_K + ks, par(g - kKSlots, kKSlots)));
         if (!ok) break;
         // a dead key's scales are zeroed, which zeroes its row whatever the codes
         const bool live = ((raw_valid[rs] >> pg) & 1) && (pc.p0 + k) * kUnitKeys + key < pc.s.len;
         const uint32_t smask = live ? 0xFFFFFFFFu : 0u;
         const uint32_t rawb = smem_addr(smem + kRawOff + rs * kRawStage);
-        const uint32_t taddr = lane_base(tmem, q) + 128 * ks;
+        const uint32_t taddr = lane_base(tmem, q) + kTK + 128 * ks;
         // a runtime loop keeps the code small (the tile's roles share each
         // SM sub-partition's instruction cache); two operand sets in turn, so
         // that each step's loads are issued before the previous step is
@@ -429,13 +435,11 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           }
         }
         __syncwarp();
-        // the slot of this unit's V^T (allocation 2g + 1) is free once the
-        // QK of unit g - 1 (allocation 2g - 2) has completed
-        const int64_t al = 2 * g + 1;
-        const int vs = slot_of(al);
-        if (al >= 3) ok = waitw(V_FREE_K + vs, use_parity(al - 3));
+        // the V^T slot's previous user is the P.V of unit g - kVSlots
+        const int vs = static_cast<int>(g % kVSlots);
+        if (g >= kVSlots) ok = waitw(V_FREE_V + vs, par(g - kVSlots, kVSlots));
         if (!ok) break;
-        const uint32_t taddr = lane_base(tmem, q) + 128 * vs;
+        const uint32_t taddr = lane_base(tmem, q) + kTV + 128 * vs;
         // operands of page j: its 8 pair scales and 8 code pairs
         struct VOps {
           uint4 s0, s1;
@@ -499,12 +503,11 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       for (int k = 0; ok && k < pc.n; ++k, ++g) {
         if (qk) {
           const int sb = static_cast<int>(g & 1);
-          const int64_t al = 2 * g;  // K of unit g
-          const int ks = slot_of(al);
-          ok = waitw(V_FULL_K + ks, use_parity(al)) && (g < 2 || waitw(V_S_FREE + sb, par(g - 2, 2)));
+          const int ks = static_cast<int>(g % kKSlots);
+          ok = waitw(V_FULL_K + ks, par(g, kKSlots)) && (g < 2 || waitw(V_S_FREE + sb, par(g - 2, 2)));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d = tmem + kTS + 32 * sb, a0 = tmem + 128 * ks;
+          const uint32_t d = tmem + kTS + 32 * sb, a0 = tmem + kTK + 128 * ks;
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)  // 16 dims: 8 TMEM columns of K, 2 core matrices (256 B) of Q^T
@@ -515,13 +518,12 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           __syncwarp();
         } else {
           const int pb = static_cast<int>(g % kPStages);
-          const int64_t al = 2 * g + 1;  // V^T of unit g
-          const int vs = slot_of(al);
-          ok = waitw(V_FULL_V + vs, use_parity(al)) && waitw(V_P_FULL + pb, par(g, kPStages));
+          const int vs = static_cast<int>(g % kVSlots);
+          ok = waitw(V_FULL_V + vs, par(g, kVSlots)) && waitw(V_P_FULL + pb, par(g, kPStages));
           if (!ok) break;
           tc_fence_after();
           const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(pb * (kPBytes >> 4));
-          const uint32_t a0 = tmem + 128 * vs;
+          const uint32_t a0 = tmem + kTV + 128 * vs;
           const uint32_t acc = k > 0 ? 1u : 0u;
           if (elect_one()) {
             // the two halves' products interleaved: two independent
@@ -565,12 +567,17 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     float* xchg = reinterpret_cast<float*>(smem + kXchgOff);
     volatile uint32_t* flags = reinterpret_cast<uint32_t*>(smem + kFlagOff);
     const uint32_t lb = lane_base(tmem, q);
-    // meeting: every warp posts bits, all read the OR and the AND
+    // meeting: every warp posts bits, all read the OR and the AND.  The
+    // posts alternate between two flag sets, so one barrier suffices: a
+    // warp posts into a set again only two meetings later, after every warp
+    // has passed the meeting in between (and so has read that set).
+    uint32_t meets = 0;
     auto meet = [&](uint32_t bits, uint32_t* all_and, uint32_t* any_or) {
-      if (lane == 0) flags[q] = bits;
+      volatile uint32_t* f = flags + 4 * (meets & 1);
+      ++meets;
+      if (lane == 0) f[q] = bits;
       named_bar_sync(1, 128);
-      const uint32_t f0 = flags[0], f1 = flags[1], f2 = flags[2], f3 = flags[3];
-      named_bar_sync(1, 128);  // all have read before the next post
+      const uint32_t f0 = f[0], f1 = f[1], f2 = f[2], f3 = f[3];
       *all_and = f0 & f1 & f2 & f3;
       *any_or = f0 | f1 | f2 | f3;
     };
@@ -633,13 +640,16 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         auto load_x = [&]() {
           uint32_t sr[kRowsN];
           tmem_ld32(lb + kTS + 32 * sb, sr);
+          float4 b4[kRowsN / 4];  // the bases, read while the TMEM load is in flight
+#pragma unroll
+          for (int r4 = 0; r4 < kRowsN / 4; ++r4) b4[r4] = reinterpret_cast<const float4*>(basev)[r4];
           tmem_wait_ld();
 #pragma unroll
-          for (int r4 = 0; r4 < kRowsN; r4 += 4) {
-            const float4 b4 = *reinterpret_cast<const float4*>(basev + r4);
-            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[r4 + e] = fmaf(__uint_as_float(sr[r4 + e]), a.qk_scale_log2, -bv[e]);
+          for (int r4 = 0; r4 < kRowsN / 4; ++r4) {
+            x[4 * r4] = fmaf(__uint_as_float(sr[4 * r4]), a.qk_scale_log2, -b4[r4].x);
+            x[4 * r4 + 1] = fmaf(__uint_as_float(sr[4 * r4 + 1]), a.qk_scale_log2, -b4[r4].y);
+            x[4 * r4 + 2] = fmaf(__uint_as_float(sr[4 * r4 + 2]), a.qk_scale_log2, -b4[r4].z);
+            x[4 * r4 + 3] = fmaf(__uint_as_float(sr[4 * r4 + 3]), a.qk_scale_log2, -b4[r4].w);
           }
           if (!unmasked) {
 #pragma unroll

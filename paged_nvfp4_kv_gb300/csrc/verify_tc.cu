@@ -634,8 +634,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         const int kg = (pc.p0 + k) * kUnitKeys + key;
         // S^T column r of this key -> masked logits relative to the row's
         // exponent base, x = s * scale - base (log2 units, one FFMA); the S
-        // slot is released at the end of the unit, so it can be read again
-        // after a reduction
+        // slot is released once no reduction can read it again
         const bool unmasked = (pc.p0 + k + 1) * kUnitKeys <= vis_all;  // uniform over the CTA
         auto load_x = [&]() {
           uint32_t sr[kRowsN];
@@ -740,6 +739,11 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           break;
         }
         if (!ok) continue;  // reported at the next meeting
+        // S^T of this unit has been read for the last time: free its slot
+        // for the QK two units on
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(V_S_FREE + sb));
         // p = 2^x (at most 2^threshold; 0 for masked keys)
 #pragma unroll
         for (int r = 0; r < kRowsN; ++r) {
@@ -761,10 +765,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           fence_proxy_async();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bar(V_P_FULL + pb));
-            mbar_arrive(bar(V_S_FREE + sb));
-          }
+          if (lane == 0) mbar_arrive(bar(V_P_FULL + pb));
         }
       }
       if (!(all_and & 1u)) break;

@@ -429,15 +429,23 @@ template <int NTW>
 __device__ __forceinline__ void pv_nvfp4(uint32_t sb, int lane, WarpState<NTW>& st,
                                          const uint32_t (&pb)[NTW][2], int page_lim) {
   const int gid = lane >> 2, tig = lane & 3;
-  // scale pairs (token 2p, token 2p+1) of a block; masked tokens scale to 0
-  auto sbyte = [&](int t, int blk) -> uint32_t {
-    return t < page_lim ? lds8(sb + swz128(34 + (t >> 3), (t & 7) * 16 + blk)) : 0u;
-  };
+  // scale pairs (token 2p, token 2p+1) of a block; tokens past page_lim
+  // scale to 0 (their codes and scales may be stale)
   const int t0 = 2 * tig, t2 = 2 * tig + 8;
-  const uint32_t s_a_lo = e4m3x2_to_f16x2(sbyte(t0, gid) | (sbyte(t0 + 1, gid) << 8));
-  const uint32_t s_a_hi = e4m3x2_to_f16x2(sbyte(t0, 8 + gid) | (sbyte(t0 + 1, 8 + gid) << 8));
-  const uint32_t s_b_lo = e4m3x2_to_f16x2(sbyte(t2, gid) | (sbyte(t2 + 1, gid) << 8));
-  const uint32_t s_b_hi = e4m3x2_to_f16x2(sbyte(t2, 8 + gid) | (sbyte(t2 + 1, 8 + gid) << 8));
+  auto sbyte = [&](int t, int blk) -> uint32_t { return lds8(sb + swz128(34 + (t >> 3), (t & 7) * 16 + blk)); };
+  uint32_t b[8] = {sbyte(t0, gid), sbyte(t0 + 1, gid), sbyte(t0, 8 + gid), sbyte(t0 + 1, 8 + gid),
+                   sbyte(t2, gid), sbyte(t2 + 1, gid), sbyte(t2, 8 + gid), sbyte(t2 + 1, 8 + gid)};
+  if (page_lim < 16) {  // a partial or missing page (uniform over the warp)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = (i < 4 ? t0 : t2) + (i & 1);
+      if (t >= page_lim) b[i] = 0u;
+    }
+  }
+  const uint32_t s_a_lo = e4m3x2_to_f16x2(prmt(b[0], b[1], 0x0040u));
+  const uint32_t s_a_hi = e4m3x2_to_f16x2(prmt(b[2], b[3], 0x0040u));
+  const uint32_t s_b_lo = e4m3x2_to_f16x2(prmt(b[4], b[5], 0x0040u));
+  const uint32_t s_b_hi = e4m3x2_to_f16x2(prmt(b[6], b[7], 0x0040u));
   // pair row p = box rows 18 + 2p (dims 0..127) and 19 + 2p (dims 128..255)
   const uint4 a_lo = lds128(sb + swz128(18 + 2 * tig, 16 * gid));
   const uint4 a_hi = lds128(sb + swz128(19 + 2 * tig, 16 * gid));
@@ -876,16 +884,18 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int32_t mask_from = a.causal ? pc.s.len - pc.s.qlen + 1 : pc.s.len;  // first key some row cannot see
     // units of this piece owned by this warp, NP per iteration: i, i + S, ...
     // (missing trailing units are stand-ins for unit i, fully masked)
-    constexpr int64_t S = P::kStreams;
-    const int64_t end = pc.i0 + pc.n;
-    int64_t i = pc.i0 + ((stream - pc.i0 % S) % S + S) % S;
+    // (32-bit: i0 counts the CTA's own units)
+    constexpr int32_t S = P::kStreams;
+    const int32_t i0 = static_cast<int32_t>(pc.i0);
+    const int32_t end = i0 + pc.n;
+    int32_t i = i0 + ((stream - i0 % S) % S + S) % S;
     // stage and phase parity of unit i, advanced with 32-bit arithmetic
     // (NP * S <= kStages, so one step wraps the ring at most once)
     static_assert(NP * S <= P::kStages, "one iteration wraps the stage ring at most once");
-    int i_stage = static_cast<int>(i % P::kStages);
+    int i_stage = i % P::kStages;
     uint32_t i_par = static_cast<uint32_t>((i / P::kStages) & 1);
     for (; i < end; i += NP * S) {
-      int64_t u[NP];
+      int32_t u[NP];
       bool here[NP];
       int st_idx[NP];
       bool okw = !*abort_flag;
@@ -893,7 +903,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int pg = 0; pg < NP; ++pg) {
         here[pg] = i + pg * S < end;
         u[pg] = here[pg] ? i + pg * S : i;
-        int idx = i_stage + (here[pg] ? pg * static_cast<int>(S) : 0);
+        int idx = i_stage + (here[pg] ? pg * S : 0);
         uint32_t par = i_par;
         if (idx >= P::kStages) {
           idx -= P::kStages;
@@ -904,7 +914,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
       // one outcome per warp: the MMAs below need every lane
       okw = __all_sync(0xffffffffu, okw);
-      i_stage += NP * static_cast<int>(S);
+      i_stage += NP * S;
       if (i_stage >= P::kStages) {
         i_stage -= P::kStages;
         i_par ^= 1u;
@@ -919,7 +929,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       uint32_t sb[NP];
 #pragma unroll
       for (int pg = 0; pg < NP; ++pg) {
-        const int32_t page_idx = pc.p0 + static_cast<int32_t>(u[pg] - pc.i0);
+        const int32_t page_idx = pc.p0 + (u[pg] - i0);
         key0[pg] = page_idx * 16;
         const bool live = here[pg] && stage_valid[st_idx[pg]];
         page_lim[pg] = live ? pc.s.len - key0[pg] : 0;  // valid tokens in the page

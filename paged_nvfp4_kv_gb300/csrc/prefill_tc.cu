@@ -436,12 +436,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           // raw row slot / 8 (record row 16 + slot / 8), bytes 16 (slot % 8) ..
           if (warp < kDequantWarp0 + 4) {
             const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + P::kTmemSfb + ks * 16;
-            store_scale_factors(taddr, lane, [&](int n, int c) -> uint32_t {
-              if (n >= kBlockKeys) return 0u;
-              const int pg = n >> 4, slot = n & 15;
-              if (!((valid >> pg) & 1)) return 0u;  // a missing page scales to zero
-              return lds32(raw + pg * P::kRawPageBytes + swz128(slot >> 3, (slot & 7) * 16 + 4 * c));
-            });
+            // lane l reads the whole 16-byte chunks of keys l and l + 32 (each
+            // quarter-warp then reads 128 distinct bytes) and stores them in
+            // the layout store_scale_factors describes
+            uint4 kc[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int n = lane + 32 * j, pg = n >> 4, slot = n & 15;
+              kc[j] = lds128(raw + pg * P::kRawPageBytes + swz128(slot >> 3, (slot & 7) * 16));
+              if (!((valid >> pg) & 1)) kc[j] = make_uint4(0, 0, 0, 0);  // a missing page scales to zero
+            }
+            // column 4c + j of this lane = the scale word of row lane + 32 j,
+            // K-chunk c (rows 64 .. 127 are not keys of the block: zero)
+            const uint32_t cw[2][4] = {{kc[0].x, kc[0].y, kc[0].z, kc[0].w}, {kc[1].x, kc[1].y, kc[1].z, kc[1].w}};
+            uint32_t r[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) r[4 * c + j] = j < 2 ? cw[j][c] : 0u;
+            tmem_st16(taddr, r);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();

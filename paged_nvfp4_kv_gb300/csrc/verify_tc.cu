@@ -121,6 +121,25 @@ constexpr uint32_t kTmemColsV = 512;
 constexpr uint32_t kTK = 0, kTV = 128 * kKSlots, kTS = 384, kTO = 448;
 static_assert(kTV + 128 * kVSlots <= kTS, "TMEM plan: K and V^T slots overlap S^T");
 
+// Two fp32 lanes per instruction (packed f32x2 on the FMA pipe); each lane
+// is the IEEE operation of its scalar form, so results are bitwise the same.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rc, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; mov.b64 rc, {%6, %7};"
+      " fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
+      " add.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 __device__ __forceinline__ uint64_t* vbar(uint8_t* smem, int i) {
   return reinterpret_cast<uint64_t*>(smem + kBarOffV) + i;
 }
@@ -643,12 +662,17 @@ __global__ void __launch_bounds__(kThreadsV, 1)
 #pragma unroll
           for (int r4 = 0; r4 < kRowsN / 4; ++r4) b4[r4] = reinterpret_cast<const float4*>(basev)[r4];
           tmem_wait_ld();
+          const float2 sc2 = make_float2(a.qk_scale_log2, a.qk_scale_log2);
 #pragma unroll
           for (int r4 = 0; r4 < kRowsN / 4; ++r4) {
-            x[4 * r4] = fmaf(__uint_as_float(sr[4 * r4]), a.qk_scale_log2, -b4[r4].x);
-            x[4 * r4 + 1] = fmaf(__uint_as_float(sr[4 * r4 + 1]), a.qk_scale_log2, -b4[r4].y);
-            x[4 * r4 + 2] = fmaf(__uint_as_float(sr[4 * r4 + 2]), a.qk_scale_log2, -b4[r4].z);
-            x[4 * r4 + 3] = fmaf(__uint_as_float(sr[4 * r4 + 3]), a.qk_scale_log2, -b4[r4].w);
+            const float2 lo = ffma2(make_float2(__uint_as_float(sr[4 * r4]), __uint_as_float(sr[4 * r4 + 1])), sc2,
+                                    make_float2(-b4[r4].x, -b4[r4].y));
+            const float2 hi = ffma2(make_float2(__uint_as_float(sr[4 * r4 + 2]), __uint_as_float(sr[4 * r4 + 3])),
+                                    sc2, make_float2(-b4[r4].z, -b4[r4].w));
+            x[4 * r4] = lo.x;
+            x[4 * r4 + 1] = lo.y;
+            x[4 * r4 + 2] = hi.x;
+            x[4 * r4 + 3] = hi.y;
           }
           if (!unmasked) {
 #pragma unroll
@@ -746,9 +770,12 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (lane == 0) mbar_arrive(bar(V_S_FREE + sb));
         // p = 2^x (at most 2^threshold; 0 for masked keys)
 #pragma unroll
-        for (int r = 0; r < kRowsN; ++r) {
+        for (int r = 0; r < kRowsN; r += 2) {
           x[r] = fast_exp2(x[r]);
-          l[r] += x[r];
+          x[r + 1] = fast_exp2(x[r + 1]);
+          const float2 s2 = fadd2(make_float2(l[r], l[r + 1]), make_float2(x[r], x[r + 1]));
+          l[r] = s2.x;
+          l[r + 1] = s2.y;
         }
         // P^T slot pb was last read by the P.V of unit g - kPStages
         if (g >= kPStages) ok = waitw(V_PV_DONE + pb, par(g - kPStages, kPStages));

@@ -93,6 +93,7 @@ struct Plan<false> {
   static constexpr int kQBytes = 0, kSfaXBytes = 0;
   static constexpr uint32_t kTmemQ = 384;                // fp16 Q, two per column: 384 .. 511
   static constexpr uint32_t kTmemSfb = 0;
+  static constexpr uint32_t kTmemP = 0;                  // P lives in shared memory
 };
 
 // FP4 QK: K codes go straight from the pool into an FP4 ring (one 16-row TMA
@@ -113,6 +114,9 @@ struct Plan<true> {
   // ones per K stage
   static constexpr uint32_t kTmemSfa = 384;
   static constexpr uint32_t kTmemSfb = 400;
+  // P (fp16, two per column, 32 columns per stage): the A operand of P V
+  // straight from TMEM, so no shared-memory P ring
+  static constexpr uint32_t kTmemP = 448;
 };
 
 template <bool FP4Q>
@@ -120,7 +124,7 @@ struct Layout {
   using P = Plan<FP4Q>;
   static constexpr int kRawStageBytes = kBlockPages * P::kRawPageBytes;
   static constexpr int kVBytes = 256 * kBlockKeys * 2;   // fp16 V^T [256 dims][64 keys]
-  static constexpr int kPBytes = 128 * kBlockKeys * 2;   // fp16 P [128 rows][64 keys]
+  static constexpr int kPBytes = FP4Q ? 0 : 128 * kBlockKeys * 2;  // fp16 P [128 rows][64 keys] (FP4: in TMEM)
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + P::kKStages * P::kKBytes;
   static constexpr int kPOff = kVOff + P::kVStages * kVBytes;
@@ -156,7 +160,8 @@ struct Layout {
   static constexpr uint32_t kTmemS = 0;
   static constexpr uint32_t kTmemO = P::kSStages * kBlockKeys;
   static_assert(kTmemO + 256 <= 384, "TMEM plan: S ring and O");
-  static_assert(FP4Q ? P::kTmemSfb + 16 * P::kKStages <= kTmemCols : P::kTmemQ + 128 <= kTmemCols,
+  static_assert(FP4Q ? P::kTmemSfb + 16 * P::kKStages <= P::kTmemP && P::kTmemP + 32 * P::kPStages <= kTmemCols
+                     : P::kTmemQ + 128 <= kTmemCols,
                 "TMEM plan too large");
 };
 
@@ -642,8 +647,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acc = j > 0 ? 1u : 0u;
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kBlockKeys / 16; ++kk)  // 16 keys = 2 core matrices (256 B) of P and of V^T
-              umma_f16(tmem + L::kTmemO, pdesc + 16 * kk, vdesc + 16 * kk, idesc, kk > 0 ? 1u : acc);
+            for (int kk = 0; kk < kBlockKeys / 16; ++kk) {  // 16 keys = 2 core matrices (256 B) of P and of V^T
+              if constexpr (FP4Q)  // P from TMEM: 8 columns per 16 keys
+                umma_f16_ta(tmem + L::kTmemO, tmem + P::kTmemP + 32 * ps + 8 * kk, vdesc + 16 * kk, idesc,
+                            kk > 0 ? 1u : acc);
+              else
+                umma_f16(tmem + L::kTmemO, pdesc + 16 * kk, vdesc + 16 * kk, idesc, kk > 0 ? 1u : acc);
+            }
             umma_commit(bar(L::B_V_FREE + vs));
             umma_commit(bar(L::B_PV_DONE + ps));
           }
@@ -842,12 +852,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_warp(L::B_PV_DONE + ps, ring_parity(g - P::kPStages, P::kPStages));
           if (!ok) break;
         }
-        uint8_t* pt = smem + L::kPOff + ps * L::kPBytes;
+        if constexpr (FP4Q) {
+          // the row's 64 fp16 probabilities into its TMEM lane
+          uint32_t h0[16], h1[16];
 #pragma unroll
-        for (int c = 0; c < kBlockKeys / 8; ++c)
-          *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
-              make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-        fence_proxy_async();
+          for (int i = 0; i < 16; ++i) {
+            h0[i] = ph[i];
+            h1[i] = ph[16 + i];
+          }
+          tmem_st16(lane_addr + P::kTmemP + 32 * ps, h0);
+          tmem_st16(lane_addr + P::kTmemP + 32 * ps + 16, h1);
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          uint8_t* pt = smem + L::kPOff + ps * L::kPBytes;
+#pragma unroll
+          for (int c = 0; c < kBlockKeys / 8; ++c)
+            *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
+                make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+          fence_proxy_async();
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::B_P_FULL + ps));
       }

@@ -18,12 +18,15 @@
 //   dequant warps   widen K to fp16 [64 keys][256 dims] and V to fp16
 //                   V^T [256 dims][64 keys] (E2M1 x E4M3 is exact in fp16),
 //                   both in the no-swizzle K-major core-matrix layout
-//   MMA thread      S = Q K^T   (M 128, N 64, K 256)  -> TMEM ring, with Q
+//   MMA warps       S = Q K^T   (M 128, N 64, K 256)  -> TMEM ring, with Q
 //                               (fp16) held in TMEM as the A operand, so
 //                               shared memory feeds only K
-//                   O += P V    (M 128, N 256, K 64)  -> TMEM
+//                   O += P V    (M 128, N 256, K 64)  -> TMEM, with P the A
+//                               operand in TMEM
 //   softmax warps   one row per thread: tcgen05.ld of S, online softmax,
-//                   P (fp16) -> shared memory; O is rescaled in TMEM only when
+//                   P (fp16) -> TMEM (tcgen05.st into the S slot it came
+//                   from, or with FP4 queries into columns of its own); O is
+//                   rescaled in TMEM only when
 //                   a row's running maximum grows by more than 2^8, so the
 //                   exponentials stay below 256 and most blocks need no
 //                   rescale (the row sum adds the fp32 exponentials; P V
@@ -84,7 +87,7 @@ struct Plan;
 // page); K is widened into an fp16 ring; Q (fp16) lives in TMEM.
 template <>
 struct Plan<false> {
-  static constexpr int kRawStages = 3, kKStages = 2, kVStages = 2, kSStages = 2, kPStages = 2;
+  static constexpr int kRawStages = 4, kKStages = 2, kVStages = 2, kSStages = 2, kPStages = 2;
   static constexpr int kRawRows = 36;                    // record rows in a raw page slot
   static constexpr int kRawRow0 = 0;                     // record row of raw row 0
   static constexpr int kRawPageBytes = 5120;             // 4,608-byte record, 1,024-aligned slot
@@ -93,7 +96,10 @@ struct Plan<false> {
   static constexpr int kQBytes = 0, kSfaXBytes = 0;
   static constexpr uint32_t kTmemQ = 384;                // fp16 Q, two per column: 384 .. 511
   static constexpr uint32_t kTmemSfb = 0;
-  static constexpr uint32_t kTmemP = 0;                  // P lives in shared memory
+  // P (fp16, two per column) overwrites the first 32 columns of the S slot
+  // it was computed from (TMEM has no other room); that slot then waits for
+  // the P V of its block, not for the softmax's read, before the next QK
+  static constexpr uint32_t kTmemP = 0, kPStrideCols = kBlockKeys;
 };
 
 // FP4 QK: K codes go straight from the pool into an FP4 ring (one 16-row TMA
@@ -114,9 +120,8 @@ struct Plan<true> {
   // ones per K stage
   static constexpr uint32_t kTmemSfa = 384;
   static constexpr uint32_t kTmemSfb = 400;
-  // P (fp16, two per column, 32 columns per stage): the A operand of P V
-  // straight from TMEM, so no shared-memory P ring
-  static constexpr uint32_t kTmemP = 448;
+  // P (fp16, two per column, 32 columns per stage) in its own columns
+  static constexpr uint32_t kTmemP = 448, kPStrideCols = 32;
 };
 
 template <bool FP4Q>
@@ -124,11 +129,9 @@ struct Layout {
   using P = Plan<FP4Q>;
   static constexpr int kRawStageBytes = kBlockPages * P::kRawPageBytes;
   static constexpr int kVBytes = 256 * kBlockKeys * 2;   // fp16 V^T [256 dims][64 keys]
-  static constexpr int kPBytes = FP4Q ? 0 : 128 * kBlockKeys * 2;  // fp16 P [128 rows][64 keys] (FP4: in TMEM)
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + P::kKStages * P::kKBytes;
-  static constexpr int kPOff = kVOff + P::kVStages * kVBytes;
-  static constexpr int kRawOff = kPOff + P::kPStages * kPBytes;
+  static constexpr int kRawOff = kVOff + P::kVStages * kVBytes;  // (P is the A operand of P V in TMEM)
   static constexpr int kQOff = kRawOff + P::kRawStages * kRawStageBytes;  // FP4 Q codes
   static constexpr int kSfaXOff = kQOff + P::kQBytes;
   static constexpr int kScrOff = kSfaXOff + P::kSfaXBytes;  // per dequant warp: V scales
@@ -161,8 +164,8 @@ struct Layout {
   static constexpr uint32_t kTmemO = P::kSStages * kBlockKeys;
   static_assert(kTmemO + 256 <= 384, "TMEM plan: S ring and O");
   static_assert(FP4Q ? P::kTmemSfb + 16 * P::kKStages <= P::kTmemP && P::kTmemP + 32 * P::kPStages <= kTmemCols
-                     : P::kTmemQ + 128 <= kTmemCols,
-                "TMEM plan too large");
+                     : P::kTmemQ + 128 <= kTmemCols && P::kTmemP == kTmemS && P::kPStages == P::kSStages,
+                "TMEM plan too large (or P not aliasing the S ring)");
 };
 
 struct PrefillArgs {
@@ -595,7 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t kdesc0 =
         FP4Q ? smem_desc_sw128(smem_addr(smem + L::kKOff)) : smem_desc(smem_addr(smem + L::kKOff), 128, 4096);
     const uint64_t qdesc0 = FP4Q ? smem_desc_sw128(smem_addr(smem + L::kQOff)) : 0;
-    const uint64_t pdesc0 = smem_desc(smem_addr(smem + L::kPOff), 128, kBlockKeys * 16);
     const uint64_t vdesc0 = smem_desc(smem_addr(smem + L::kVOff), 128, kBlockKeys * 16);
     int64_t gb = 0;  // first block of the current tile
     int64_t tcount = 0;
@@ -612,7 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ks = static_cast<int>(g % P::kKStages), ss = static_cast<int>(g % P::kSStages);
           ok = wait_warp(L::B_K_FULL + ks, ring_parity(g, P::kKStages)) &&
                (!FP4Q || wait_warp(L::B_KC_FULL + ks, ring_parity(g, P::kKStages))) &&
-               (g < P::kSStages || wait_warp(L::B_S_FREE + ss, ring_parity(g - P::kSStages, P::kSStages)));
+               (g < P::kSStages ||
+                (FP4Q ? wait_warp(L::B_S_FREE + ss, ring_parity(g - P::kSStages, P::kSStages))
+                      // P of block g - 2 sits in this S slot: wait for its P V
+                      : wait_warp(L::B_PV_DONE + ss, ring_parity(g - P::kSStages, P::kPStages))));
           if (!ok) break;
           tc_fence_after();
           const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(ks * (P::kKBytes >> 4));
@@ -642,17 +647,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                wait_warp(L::B_V_FULL + vs, ring_parity(g, P::kVStages));
           if (!ok) break;
           tc_fence_after();
-          const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(ps * (L::kPBytes >> 4));
           const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(vs * (L::kVBytes >> 4));
           const uint32_t acc = j > 0 ? 1u : 0u;
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kBlockKeys / 16; ++kk) {  // 16 keys = 2 core matrices (256 B) of P and of V^T
-              if constexpr (FP4Q)  // P from TMEM: 8 columns per 16 keys
-                umma_f16_ta(tmem + L::kTmemO, tmem + P::kTmemP + 32 * ps + 8 * kk, vdesc + 16 * kk, idesc,
-                            kk > 0 ? 1u : acc);
-              else
-                umma_f16(tmem + L::kTmemO, pdesc + 16 * kk, vdesc + 16 * kk, idesc, kk > 0 ? 1u : acc);
+              // P from TMEM: 8 columns per 16 keys
+              umma_f16_ta(tmem + L::kTmemO, tmem + P::kTmemP + P::kPStrideCols * ps + 8 * kk, vdesc + 16 * kk,
+                          idesc, kk > 0 ? 1u : acc);
             }
             umma_commit(bar(L::B_V_FREE + vs));
             umma_commit(bar(L::B_PV_DONE + ps));
@@ -784,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::B_S_FREE + ss));
+        if (FP4Q && lane == 0) mbar_arrive(bar(L::B_S_FREE + ss));
         // the row maximum of the raw logits over the visible keys (masked
         // keys become -inf); the logit scale is positive, so the maximum of
         // the scaled logits is the scaled maximum
@@ -852,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_warp(L::B_PV_DONE + ps, ring_parity(g - P::kPStages, P::kPStages));
           if (!ok) break;
         }
-        if constexpr (FP4Q) {
+        {
           // the row's 64 fp16 probabilities into its TMEM lane
           uint32_t h0[16], h1[16];
 #pragma unroll
@@ -860,17 +862,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             h0[i] = ph[i];
             h1[i] = ph[16 + i];
           }
-          tmem_st16(lane_addr + P::kTmemP + 32 * ps, h0);
-          tmem_st16(lane_addr + P::kTmemP + 32 * ps + 16, h1);
+          tmem_st16(lane_addr + P::kTmemP + P::kPStrideCols * ps, h0);
+          tmem_st16(lane_addr + P::kTmemP + P::kPStrideCols * ps + 16, h1);
           tmem_wait_st();
           tc_fence_before();
-        } else {
-          uint8_t* pt = smem + L::kPOff + ps * L::kPBytes;
-#pragma unroll
-          for (int c = 0; c < kBlockKeys / 8; ++c)
-            *reinterpret_cast<uint4*>(pt + core_off(r, 8 * c, kBlockKeys)) =
-                make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-          fence_proxy_async();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::B_P_FULL + ps));

@@ -107,7 +107,7 @@ struct Plan<false> {
 // codes, V scales); Q codes live in shared memory, the scale factors in TMEM.
 template <>
 struct Plan<true> {
-  static constexpr int kRawStages = 4, kKStages = 3, kVStages = 2, kSStages = 2, kPStages = 2;
+  static constexpr int kRawStages = 4, kKStages = 3, kVStages = 3, kSStages = 2, kPStages = 2;
   static constexpr int kRawRows = 20;
   static constexpr int kRawRow0 = 16;
   static constexpr int kRawPageBytes = 3072;             // 2,560 bytes, 1,024-aligned slot

@@ -15,8 +15,9 @@
 //   S^T [128 keys x 32 rows]  = K [128 x 256] . Q^T      (16 MMAs, M128 N32 K16)
 //   O^T [256 dims x 32 rows] += V^T [256 x 128] . P^T    (2 x 8 MMAs)
 // with K and V^T widened once per unit straight into TMEM as the A operands
-// (lane = key for K, lane = dim for V^T; two fp16 per column), Q^T and P^T
-// as the B operands in shared memory, S^T and O^T accumulating in TMEM.
+// (lane = key for K; lane L = dims 2L and 2L + 1, one per half, for V^T; two
+// fp16 per column), Q^T and P^T as the B operands in shared memory, S^T and
+// O^T accumulating in TMEM.
 // Each page-head's codes are read from HBM once and widened once, whatever
 // the number of query rows.
 //
@@ -35,7 +36,8 @@
 //   producer warp 12    one 2-D TMA load per page (the head record) into a
 //                       4-stage ring
 //   warp 13             allocates TMEM, issues the QK products
-//   warp 14             issues the P.V products
+//   warp 14             issues the P.V products (both warps run their loops
+//                       warp-uniform; one elected thread issues)
 // Work is split stream-K over (sequence, KV head, unit) exactly as the decode
 // path splits its pages, with the same partial slots, so split_kv_combine
 // merges the pieces.

@@ -45,9 +45,9 @@ def _session(w):
     return s, out32, out16, lse
 
 
-def _workload(name, dtype, cached, qlen, seed=77):
+def _workload(name, dtype, cached, qlen, seed=77, **kw):
     from paged_nvfp4_kv_gb300 import workloads as W
-    return W.build(name, seed, dtype, cached, qlen)
+    return W.build(name, seed, dtype, cached, qlen, **kw)
 
 
 CASES = {
@@ -79,13 +79,19 @@ CASES = {
     # more than 64 query rows per KV head: the tensor-core tile path
     "prefill-nvfp4": ("nvfp4", [3000, 500, 77], [100, 37, 1]),
     "prefill-long-nvfp4": ("nvfp4", [40000], [300]),
+    # the verify tile's row range on NVFP4 pools at its two ends and without
+    # the causal mask: 8 query heads per KV head x 4 tokens = all 32 rows of
+    # the product's N; 3 x 3 = 9 rows, the fewest that take the tile
+    "verify-32rows-nvfp4": ("nvfp4", [900, 130, 2500], [4, 4, 1], {"num_q_heads": 32, "num_kv_heads": 4}),
+    "verify-9rows-nvfp4": ("nvfp4", [257, 1500, 64], [3, 1, 2], {"num_q_heads": 12, "num_kv_heads": 4}),
+    "verify5-noncausal-nvfp4": ("nvfp4", [700, 333, 2011], [5, 5, 2], {"causal": False}),
 }
 
 
 @pytest.fixture(scope="module", params=sorted(CASES))
 def run(request):
-    dtype, cached, qlen = CASES[request.param]
-    w = _workload(request.param, dtype, cached, qlen)
+    dtype, cached, qlen, *extra = CASES[request.param]
+    w = _workload(request.param, dtype, cached, qlen, **(extra[0] if extra else {}))
     s, out32, out16, lse = _session(w)
     return w, s, out32, out16, lse
 

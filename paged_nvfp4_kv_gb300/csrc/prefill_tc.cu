@@ -76,10 +76,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 // Shared-memory and TMEM plan of each variant (offsets from a 1,024-byte
-// aligned base).  Ring depths: the QK of block g waits for the softmax of
-// block g - kSStages to have loaded its S slot, so QK runs up to kSStages
-// blocks ahead of the softmax, and the softmax of a block overlaps the P V of
-// the one before.
+// aligned base).  Ring depths: the QK of block g waits for its S slot to be
+// free -- with NVFP4 queries once the softmax of block g - kSStages has
+// loaded it, with bf16 queries (whose P overwrites the slot) once the P V of
+// that block has completed -- so QK runs up to kSStages blocks ahead, and the
+// softmax of a block overlaps the P V of the one before.
 template <bool FP4Q>
 struct Plan;
 
